@@ -1,0 +1,203 @@
+/*
+ * zipage.h — C ABI of the Compressed-PagedAttention compression pass (sm_103a).
+ *
+ * The operation is the compression step of Zipage ("Zipage: Maintain High Request Concurrency
+ * for LLM Reasoning through Compressed PagedAttention", summaries on gist.science; zh page §2.1,
+ * de page §2 "Methodik", es page §2 "Metodología", fr page §2.A–§2.E).  A request that holds
+ * N_max blocks of b tokens and has filled its last block is compressed: every cached token of
+ * every layer and KV head is scored, the top k = (N_max-1)*b per KV head are kept in their
+ * original order and rewritten compactly into the first N_max-1 blocks (or into newly
+ * allocated target blocks where the leading blocks are shared prefix blocks), and the last
+ * block is released.
+ *
+ * Conventions
+ *   - Every device buffer is allocated and owned by the caller; the library never frees
+ *     caller memory.  "device" below means a pointer into GPU global memory, "host" a pointer
+ *     into CPU memory.
+ *   - Calls that launch work are asynchronous on the given stream and return as soon as the
+ *     launch is queued.  Host-side argument errors are returned immediately and nothing is
+ *     launched.  Errors that only the GPU can see (a block id outside the pool, a seq_len or
+ *     query slot out of range, a wait that gave up) are written to the error word at the
+ *     start of the caller's workspace; the unit concerned is skipped, never half-written.
+ *     Read it with zp_read_error().
+ *   - bf16 is passed as raw 16-bit storage (`uint16_t`): the library does not depend on any
+ *     C++ bf16 type.
+ *   - KV pool layout (bf16): [num_layers][num_blocks][2][num_kv_heads][block_size][head_dim],
+ *     index 0 of the third dimension = K, 1 = V.  Each (layer, block, K|V, head) tile of
+ *     block_size*head_dim values is contiguous.
+ */
+#ifndef ZIPAGE_H
+#define ZIPAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t zp_status;
+enum {
+  ZP_OK = 0,
+  ZP_ERR_INVALID_ARG = 1,  /* a host-side argument is out of range or inconsistent */
+  ZP_ERR_NO_BLOCKS = 2,    /* the allocator cannot satisfy the request; nothing changed */
+  ZP_ERR_BAD_TABLE = 3,    /* (device) a block id, seq_len or query slot is out of range */
+  ZP_ERR_TIMEOUT = 4,      /* (device) a bounded wait inside a kernel gave up */
+  ZP_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  ZP_ERR_UNSUPPORTED = 6   /* valid arguments outside what this build implements */
+};
+
+/* Opaque stream handle: a cudaStream_t (CUstream) passed through as a pointer, NULL = legacy
+ * default stream. */
+typedef void* zp_stream;
+
+/* Method parameters.  The pages fix N_max, b and w; alpha, beta, decay and scale are readings
+ * (the pages name the three scores but print no weights). */
+typedef struct zp_params {
+  int32_t num_layers;     /* layers in the pool */
+  int32_t num_q_heads;    /* H_q */
+  int32_t num_kv_heads;   /* H_kv; H_q % H_kv == 0, G_q = H_q / H_kv query heads per KV head */
+  int32_t head_dim;       /* d: 64 or 128 */
+  int32_t block_size;     /* b: 16 or 32 tokens per block */
+  int32_t n_max;          /* N_max: block cap per request, >= 2 */
+  int32_t window;         /* w: observation-window length, 1 <= w <= (n_max-1)*b */
+  float alpha;            /* weight of the carried global score */
+  float beta;             /* weight of the redundancy score (subtracted) */
+  float decay;            /* global-score decay: G' = decay*G + attn */
+  float scale;            /* logit scale, normally 1/sqrt(d) */
+  int32_t protect_window; /* 1: the last w tokens are always kept */
+  int32_t causal;         /* 1: window row i sees keys t <= L-w+i */
+} zp_params;
+
+typedef struct zp_kv_pool {
+  void* base;             /* device, bf16, layout above; 16-byte aligned */
+  int64_t num_blocks;     /* blocks per layer */
+} zp_kv_pool;
+
+typedef struct zp_seq_meta {
+  int32_t num_requests;       /* R: requests compressed by this call */
+  int32_t max_blocks;         /* row stride of the block tables (>= n_max) */
+  const int32_t* seq_len;     /* device [R]: cached tokens; must equal n_max*b */
+  const int32_t* qslot;       /* device [R]: query slot of each request, 0 <= qslot < num_qslots */
+  const int32_t* dst_tables;  /* device [R][max_blocks]: where survivors go; equals the source
+                                 table except at target blocks (zp_plan_compress) */
+} zp_seq_meta;
+
+/* Optional per-token outputs, each device [R][num_layers][num_kv_heads][n_max*b] (row-major),
+ * any field may be NULL.  attn = window attention score, redund = Lightning redundancy,
+ * score = combined score S (+inf on protected tokens), keep = 1 if kept else 0. */
+typedef struct zp_debug {
+  float* attn;
+  float* redund;
+  float* score;
+  int32_t* keep;
+} zp_debug;
+
+/* ---------------------------------------------------------------------------------------
+ * Compression pass (zh §2.1 core mechanism; zh §2.3 cross-layer parallel compression).
+ *
+ * One launch covers every (request, layer, kv head) unit.  For unit (r, l, h) with
+ * L = n_max*b cached tokens read through block_tables[r]:
+ *   attn[t]  = mean over the w*G_q window rows (i, g) of softmax_t(scale*<q_{i,g}, k_t>),
+ *              row i being the query of position L-w+i (causal if params.causal);
+ *   R[t]     = mean cosine similarity of k_t to the other keys of its block (Lightning);
+ *   S[t]     = attn[t] + alpha*G[t] - beta*R[t]  (+inf for the last w if protect_window);
+ *   keep the k = (n_max-1)*b tokens first in (S desc, t asc); survivor j (ascending t) is
+ *   copied bit for bit to logical slot j of dst_tables[r]; G'[j] = decay*G[src_j] + attn[src_j]
+ *   for j < k and 0 for k <= j < L.
+ * Arguments
+ *   pool          device KV pool, read through block_tables and written through dst_tables.
+ *   block_tables  device [R][max_blocks] int32, physical block of each logical block.
+ *   meta          host struct with device pointers (see zp_seq_meta).
+ *   obs_q         device bf16 [num_qslots][num_layers][w][H_q][d]: the window queries;
+ *                 16-byte aligned.
+ *   num_qslots    M, number of query slots in obs_q and global_scores.
+ *   global_scores device fp32 [num_qslots][num_layers][H_kv][n_max*b], updated in place.
+ *   params        host.
+ *   dbg           host struct or NULL.
+ *   workspace     device, >= zp_compress_workspace_size() bytes, 256-byte aligned; holds the
+ *                 error word.  The call clears it before the kernel runs.
+ *   stream        stream to launch on.
+ * Source and destination blocks of different requests must not overlap (shared prefix
+ * blocks are only read).  Returns ZP_OK once queued.
+ * --------------------------------------------------------------------------------------- */
+zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
+                      const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
+                      const zp_params* params, const zp_debug* dbg, void* workspace,
+                      size_t workspace_bytes, zp_stream stream);
+
+/* Bytes of workspace zp_compress needs (the device error word and its padding). */
+size_t zp_compress_workspace_size(const zp_params* params, int32_t num_requests);
+
+/* ---------------------------------------------------------------------------------------
+ * Paged decode attention over the (compacted) cache — the consumer that runs on the main
+ * stream while compression runs on a side stream (zh §2.1 asynchronous compression and
+ * decoding; fr §2.D).
+ *   out[r][qh] = softmax_t(scale*<q[r][qh], k_t>) . v_t over t < seq_lens[r], with keys and
+ *   values of kv head qh / G_q of `layer`, read through block_tables[r].
+ * q, out: device bf16 [B][H_q][d]; block_tables device [B][max_blocks]; seq_lens device [B]
+ * (1 <= seq_len <= max_blocks*b).  workspace >= zp_paged_decode_workspace_size() bytes,
+ * 256-byte aligned (split-KV partials + error word).
+ * --------------------------------------------------------------------------------------- */
+zp_status zp_paged_decode_attn(const zp_kv_pool* pool, int32_t layer, const uint16_t* q,
+                               const int32_t* block_tables, const int32_t* seq_lens, int32_t B,
+                               int32_t max_blocks, uint16_t* out, const zp_params* params,
+                               void* workspace, size_t workspace_bytes, zp_stream stream);
+
+size_t zp_paged_decode_workspace_size(const zp_params* params, int32_t B, int32_t max_blocks);
+
+/* Synchronises `stream`, copies the error word at the start of `workspace` to *out_status and
+ * clears it.  Returns ZP_ERR_CUDA if the copy fails. */
+zp_status zp_read_error(void* workspace, zp_stream stream, zp_status* out_status);
+
+/* ---------------------------------------------------------------------------------------
+ * Block allocator with reference counts (the PagedAttention block manager with prefix
+ * sharing: zh §2.2, de §2 "Prefix Caching", fr §2.C).  Host only.  Free ids are handed out
+ * lowest first so that plans are deterministic.  Every call is all-or-nothing.
+ * --------------------------------------------------------------------------------------- */
+typedef struct zp_alloc zp_alloc;
+
+zp_status zp_alloc_create(int64_t num_blocks, zp_alloc** out);
+void zp_alloc_destroy(zp_alloc* a);
+/* n fresh blocks (refcount 1) into ids[n]; ZP_ERR_NO_BLOCKS if fewer than n are free. */
+zp_status zp_alloc_blocks(zp_alloc* a, int32_t n, int32_t* ids);
+/* Marks the given free ids as allocated (refcount 1), e.g. to restore a saved state;
+ * ZP_ERR_INVALID_ARG if any is out of range, repeated or not free. */
+zp_status zp_alloc_reserve(zp_alloc* a, const int32_t* ids, int32_t n);
+zp_status zp_incref(zp_alloc* a, const int32_t* ids, int32_t n);
+/* A block whose refcount reaches 0 becomes free.  ZP_ERR_INVALID_ARG on a free id. */
+zp_status zp_decref(zp_alloc* a, const int32_t* ids, int32_t n);
+/* Deferred decref: applied once all work queued on `stream` before this call has finished
+ * (the library records its own event).  stream may be NULL only if no CUDA work reads the
+ * blocks; then the decref is applied at once. */
+zp_status zp_decref_after(zp_alloc* a, const int32_t* ids, int32_t n, zp_stream stream);
+/* Applies the deferred decrefs whose work has finished (non-blocking). */
+zp_status zp_alloc_poll(zp_alloc* a);
+/* Waits for all deferred decrefs and applies them. */
+zp_status zp_alloc_drain(zp_alloc* a);
+int32_t zp_refcount(const zp_alloc* a, int32_t id);   /* -1 if id out of range */
+int64_t zp_num_free(const zp_alloc* a);
+int64_t zp_num_pending(const zp_alloc* a);           /* blocks waiting in deferred decrefs */
+
+/* Plan of one compression (zh §2.2 / fr §2.C target blocks).  host_tables, host_dst_tables:
+ * host [R][max_blocks].  For each request and each logical block i < n_max-1 the destination
+ * is the same physical block unless its refcount is > 1 (shared prefix block), in which case
+ * it is a freshly allocated target block.  Entries i >= n_max-1 are copied unchanged.
+ * Transactional: ZP_ERR_NO_BLOCKS leaves the allocator unchanged. */
+zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks,
+                           int32_t n_max, int32_t* host_dst_tables);
+
+/* After the compression launched on `stream`: for each request, decref every replaced shared
+ * block (old != new for i < n_max-1) and the old last block old[n_max-1], deferred until the
+ * work queued on `stream` has finished (the kernel still reads those blocks). */
+zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables,
+                             int32_t R, int32_t max_blocks, int32_t n_max, zp_stream stream);
+
+/* Library version, for the binding's sanity check. */
+int32_t zp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZIPAGE_H */
