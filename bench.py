@@ -1,0 +1,437 @@
+"""Benchmark of the Compressed-PagedAttention compression pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one compression pass (window attention, Lightning redundancy, combined score,
+per-head top-k, global-score update, in-place compaction / target-block writes) over every
+(request, layer, kv head) unit of the batch, in one fused launch, followed by the deferred
+release of the last blocks.  Default workload: the Llama-3-8B-shaped batch (64 requests x 32
+layers, 32/8 heads, d 128, b 16, N_max 128, w 32) = 2048 compressions per step.
+
+Compaction is destructive, so before every step the pool and the global scores are restored
+from a pristine device copy, outside the timed CUDA events; the 17 GB restore also evicts L2.
+Rank 0 prints one JSON line.  With torchrun (N > 1) every rank compresses its own batch of
+the same shape (data-parallel by request, no exchange step) and the time is the max over
+ranks.  `--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "compressions/s (request·layer) and achieved HBM GB/s vs GB300 roofline"
+
+
+# ------------------------------------------------------------------ helpers ----------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic bytes -------
+
+def algorithmic_bytes(batch, keep):
+    """Bytes the pass must move, per step (one launch).
+
+    K read once: L*d*2 per head; Q read once: w*G_q*d*2 per head; global score read L*4 and
+    written L*4 per head; for every moved survivor (destination physical slot differs from the
+    source slot): V read + K write + V write = 3*d*2 (moved K comes from shared memory, no
+    second read); block tables: 2*n_max*4 per (request, layer).
+    """
+    import torch
+    wl = batch.wl
+    R, nl, Hkv, d, b, L, w = (batch.inp.num_compress, wl.num_layers, wl.num_kv_heads, wl.head_dim,
+                              wl.block_size, wl.L, wl.window)
+    Gq = wl.num_q_heads // Hkv
+    heads = R * nl * Hkv
+    dev = keep.device
+    t = torch.arange(L, device=dev)
+    moved_total = 0
+    for r in range(R):
+        kp = keep[r].to(torch.int64)                           # [nl, Hkv, L]
+        j = torch.cumsum(kp, -1) - 1                           # destination slot of kept t
+        src_tab = torch.from_numpy(batch.tables[r]).to(dev).long()
+        dst_tab = torch.from_numpy(batch.dst_tables[r]).to(dev).long()
+        jj = j.clamp(min=0)
+        same = (src_tab[t // b][None, None, :] == dst_tab[jj // b]) & ((t % b)[None, None, :] == jj % b)
+        moved_total += int(((kp == 1) & ~same).sum().item())
+    per_head_fixed = L * d * 2 + w * Gq * d * 2 + 2 * L * 4
+    total = heads * per_head_fixed + moved_total * 3 * d * 2 + R * nl * 2 * wl.n_max * 4
+    return total, moved_total
+
+
+# ------------------------------------------------------------------ CPU oracle baseline -----
+
+def _oracle_task(task):
+    from oracle import zipage_oracle as O
+    pool, tables, seq, qslot, obs_q, gs, params = task
+    O.compress_pass(pool, tables, tables, seq, qslot, obs_q, gs, params)
+    return 1
+
+
+def oracle_sample_tasks(inp, batch_pool, requests, layers):
+    """Per-compression oracle inputs (one request, one layer, all kv heads), bf16 bit patterns."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_obs_gb300 import synth
+    wl = inp.wl
+    tasks = []
+    for r in requests:
+        blocks = torch.from_numpy(inp.block_tables[r, :wl.n_max].astype(np.int64)).to(batch_pool.device)
+        for l in layers:
+            pool = synth.bf16_bits(batch_pool[l:l + 1, blocks])
+            tables = np.arange(wl.n_max, dtype=np.int32)[None]
+            s = int(inp.qslot[r])
+            obs_q = synth.bf16_bits(inp.obs_q[s:s + 1, l:l + 1])
+            gs = inp.global_scores[s:s + 1, l:l + 1].cpu().numpy()
+            p = dict(wl.params(), num_layers=1)
+            tasks.append((pool, tables, np.array([wl.L], np.int32), np.array([0], np.int32), obs_q, gs, p))
+    return tasks
+
+
+def time_oracle(tasks, cores):
+    """Wall time of the oracle over the tasks on `cores` spawned processes (1 BLAS thread each)."""
+    import multiprocessing as mp
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_task, tasks[:cores])  # warm the workers (imports), untimed
+        t0 = time.perf_counter()
+        pool.map(_oracle_task, tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------ our arm -----------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from paged_kv_cache_obs_gb300 import runner, synth, zipage
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, "cuda", seed=synth.seed_of(wl) + 1000 * rank)
+    pristine_pool = inp.pool.clone()
+    pristine_gs = inp.global_scores.clone()
+    batch = runner.CompressionBatch(inp, "cuda", pool=inp.pool)
+    stream = torch.cuda.Stream()
+    compressions = inp.num_compress * wl.num_layers
+
+    # algorithmic bytes from one untimed run with the per-token keep flags
+    batch.enable_debug()
+    with torch.cuda.stream(stream):
+        batch.launch(stream=stream)
+    assert batch.error(stream) == 0
+    alg_bytes, moved = algorithmic_bytes(batch, batch.debug["keep"])
+    batch.debug = None
+
+    def restore():
+        batch.pool.copy_(pristine_pool)
+        batch.gs.copy_(pristine_gs)
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            restore()
+            batch.launch(stream=stream)
+    stream.synchronize()
+    assert batch.error(stream) == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            with torch.cuda.stream(stream):
+                restore()
+                starts[i].record(stream)
+                batch.launch(stream=stream)
+                ends[i].record(stream)
+            batch.commit(stream=stream)           # deferred release of the last blocks (host)
+            zipage.zp_alloc_drain(batch.alloc)    # ... and undo it for the next identical step
+            batch.close()
+            batch.alloc = None
+            _reset_alloc(batch, inp)
+        torch.cuda.synchronize()
+    barrier(world)
+    assert batch.error(stream) == 0
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(times) / len(times)
+    ms_max = max_over_ranks(ms, world)
+    value = compressions * world / (ms_max / 1e3)
+
+    peak, peak_kind = hbm_peak()
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    traffic = _ncu_traffic(args.workload)
+    out = {
+        "metric": METRIC, "value": value, "unit": "compressions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 K/V/Q, fp32 scores", "data": "synthetic (seeded)",
+        "config": {"workload": f"{wl.name}: {inp.num_compress} requests x {wl.num_layers} layers, "
+                               f"Hq {wl.num_q_heads}/Hkv {wl.num_kv_heads}, d {wl.head_dim}, b {wl.block_size}, "
+                               f"N_max {wl.n_max}, w {wl.window}",
+                   "compressions_per_step": compressions, "units_per_step": compressions * wl.num_kv_heads,
+                   "moved_rows_per_step": moved,
+                   "l2": "pool + global scores restored from a pristine device copy before every step "
+                         "(17 GB, outside the timed events), so L2 is flushed between steps",
+                   "parallelism": f"dp{world} (independent batches, no exchange)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} (hbm_gbs burst copy)",
+                     "kernel": "compress_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                     "launch_ms_mean": ms, "launch_ms_min": min(times)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, wl, inp, pristine_pool, pristine_gs, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = run_cpu_baseline(inp, pristine_pool, pristine_gs)
+    batch.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _reset_alloc(batch, inp):
+    import numpy as np
+    from paged_kv_cache_obs_gb300 import zipage
+    batch.alloc = zipage.zp_alloc_create(inp.pool.shape[1])
+    used = np.nonzero(inp.refcount)[0].astype(np.int32)
+    zipage.zp_alloc_reserve(batch.alloc, used)
+    extra = np.repeat(np.arange(inp.pool.shape[1], dtype=np.int32), np.maximum(inp.refcount - 1, 0))
+    if len(extra):
+        zipage.zp_incref(batch.alloc, extra)
+    batch.dst_tables = zipage.zp_plan_compress(batch.alloc, batch.tables, inp.wl.n_max)
+
+
+def _ncu_traffic(workload):
+    """DRAM bytes per launch of compress_kernel from the committed ncu summary, if it exists
+    and was taken on the current kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", f"compress_kernel_{workload}_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        import hashlib
+        src = open(os.path.join(ROOT, "paged_kv_cache_obs_gb300", "csrc", "zp_compress.cu"), "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+def run_e2e(args, wl, inp, pristine_pool, pristine_gs, world):
+    """Same metric through the public API with HOST buffers: every step copies the pool,
+    window queries, global scores and tables from pinned host memory, plans on the host,
+    compresses, and copies the compacted pool and global scores back to pinned host memory."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_obs_gb300 import runner, zipage
+    h_pool = torch.empty(pristine_pool.shape, dtype=pristine_pool.dtype, pin_memory=True)
+    h_pool.copy_(pristine_pool)
+    h_out = torch.empty_like(h_pool, pin_memory=True)
+    h_q = inp.obs_q.cpu().pin_memory()
+    h_gs = pristine_gs.cpu().pin_memory()
+    h_gs_out = torch.empty_like(h_gs, pin_memory=True)
+    h_tables = torch.from_numpy(inp.block_tables[:inp.num_compress].copy()).pin_memory()
+    batch = runner.CompressionBatch(inp, "cuda", pool=torch.empty_like(pristine_pool))
+    stream = torch.cuda.Stream()
+    steps = max(2, min(args.steps, 5))
+    bytes_in = (h_pool.numel() * 2 + h_q.numel() * 2 + h_gs.numel() * 4 + 2 * h_tables.numel() * 4
+                + 2 * inp.num_compress * 4)
+    bytes_out = h_pool.numel() * 2 + h_gs.numel() * 4
+
+    def step():
+        with torch.cuda.stream(stream):
+            batch.pool.copy_(h_pool, non_blocking=True)
+            batch.obs_q.copy_(h_q, non_blocking=True)
+            batch.gs.copy_(h_gs, non_blocking=True)
+            batch.d_tables.copy_(h_tables, non_blocking=True)
+            _reset_alloc(batch, inp)
+            batch.d_dst.copy_(torch.from_numpy(batch.dst_tables), non_blocking=False)
+            batch.launch(stream=stream)
+            batch.commit(stream=stream)
+            h_out.copy_(batch.pool, non_blocking=True)
+            h_gs_out.copy_(batch.gs, non_blocking=True)
+        stream.synchronize()
+        zipage.zp_alloc_drain(batch.alloc)
+        zipage.zp_alloc_destroy(batch.alloc)
+        batch.alloc = None
+
+    step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
+    comp = inp.num_compress * wl.num_layers * world
+    return {"value": comp / dt, "unit": "compressions/s", "h2d_bytes_per_step": int(bytes_in),
+            "d2h_bytes_per_step": int(bytes_out), "steps": steps, "ms_per_step": dt * 1e3}
+
+
+def run_cpu_baseline(inp, pool, gs):
+    wl = inp.wl
+    inp.global_scores = gs
+    cores = os.cpu_count() or 1
+    reqs = list(range(min(4, inp.num_compress)))
+    layers = list(range(wl.num_layers))
+    tasks = oracle_sample_tasks(inp, pool, reqs, layers)
+    t = time_oracle(tasks, cores)
+    return {"value": len(tasks) / t, "unit": "compressions/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(tasks)} compressions ({len(reqs)} requests x {len(layers)} layers, all "
+                      f"{wl.num_kv_heads} kv heads) of the same workload, fp64 numpy oracle, "
+                      f"{cores} spawned processes x 1 BLAS thread",
+            "seconds": t}
+
+
+# ------------------------------------------------------------------ reference arm -----------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from paged_kv_cache_obs_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    # the same inputs as our arm, drawn on the CPU for the sampled requests only
+    small = wl.scaled(num_requests=2)
+    inp = synth.make_inputs(small, "cpu", seed=synth.seed_of(wl))
+    cores = os.cpu_count() or 1
+    per_step = max(cores, 16)
+    tasks = oracle_sample_tasks(inp, inp.pool, [0, 1], list(range(wl.num_layers)))
+    tasks = (tasks * ((per_step + len(tasks) - 1) // len(tasks)))[:per_step]
+    for _ in range(args.warmup):
+        time_oracle(tasks[:cores], cores)
+    times = [time_oracle(tasks, cores) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = len(tasks) / t
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "compressions/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": f"{wl.name} (sample of {per_step} compressions per step)"},
+           "cpu_baseline": {"value": value, "unit": "compressions/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{per_step} compressions per step (request x layer, all kv heads)"},
+           "e2e": {"value": value, "unit": "compressions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

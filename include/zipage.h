@@ -175,6 +175,9 @@ zp_status zp_decref_after(zp_alloc* a, const int32_t* ids, int32_t n, zp_stream 
 zp_status zp_alloc_poll(zp_alloc* a);
 /* Waits for all deferred decrefs and applies them. */
 zp_status zp_alloc_drain(zp_alloc* a);
+/* Test hook (host-side fault injection): the nth_call-th allocating call from now returns
+ * ZP_ERR_NO_BLOCKS without changing anything; 0 disables. */
+zp_status zp_alloc_inject_failure(zp_alloc* a, int64_t nth_call);
 int32_t zp_refcount(const zp_alloc* a, int32_t id);   /* -1 if id out of range */
 int64_t zp_num_free(const zp_alloc* a);
 int64_t zp_num_pending(const zp_alloc* a);           /* blocks waiting in deferred decrefs */

@@ -1,0 +1,607 @@
+// zp_compress.cu — fused compression pass of Compressed PagedAttention for sm_103a.
+//
+// Operation (Zipage summaries on gist.science: zh §2.1 core mechanism and Lightning Redundancy
+// Score, zh §2.2 prefix-cache compatibility, zh §2.3 cross-layer parallel compression, fr §2.A
+// window always kept).  Per unit u = (request r, layer l, kv head h) with L = n_max*b cached
+// tokens:
+//   attn[t] = mean_{rows (i,g)} softmax_t(scale*<q_{i,g}, k_t>)   (row i = position L-w+i)
+//   R[t]    = mean_{j in block(t), j != t} cos(k_t, k_j)           (Lightning redundancy)
+//   S[t]    = attn[t] + alpha*G[t] - beta*R[t]                     (+inf on the protected window)
+//   keep the k = (n_max-1)*b best (S desc, t asc), copy survivor j to slot j of the dst table,
+//   G'[j] = decay*G[src_j] + attn[src_j], G'[k..L) = 0.
+//
+// GB300 mapping.  One thread-block cluster of C = ceil(L/256) CTAs per unit; CTA c owns the
+// 256 logical slots [256c, 256c+256).  Each CTA:
+//   1. TMA-loads its K rows (paged gather: one 3-D box per (block, 64-column half)) and the
+//      unit's w*G_q window queries into 128-byte-swizzled shared memory.
+//   2. tcgen05 MMA D1 = Q K^T (M=128 query rows, N=256 keys) into TMEM; each thread owns one
+//      query row and reduces its row max / exp-sum without shuffles.
+//   3. Pushes the per-row (max, sum) partials to every CTA of the cluster (DSMEM); meanwhile
+//      MMA Gram = K_h K_h^T per 128-key half gives the in-block cosine similarities
+//      (Lightning redundancy, diagonal = squared norms).
+//   4. MMA D2 = K Q^T (M=128 keys, N=128 rows): each thread owns one key and sums its
+//      normalised probabilities over the window rows without shuffles.
+//   5. Selection: per-warp, per-CTA and per-cluster candidate filtering of the E = L-k
+//      lowest (S asc, t desc) keys; every CTA derives the same eviction set.
+//   6. V rows that move are loaded into registers; a cluster barrier separates every read of
+//      the unit from every write (compaction is in place, dst <= src); K rows are written
+//      from shared memory, V rows from registers, G' from registers.
+// All waits are bounded; a failed wait or a bad table makes the whole unit skip its writes.
+#include <cstdio>
+#include <mutex>
+
+#include "zp_internal.h"
+#include "zp_ptx.cuh"
+
+namespace zp {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kKeysPerCta = 256;
+constexpr int kRows = 128;         // window rows, padded: MMA M of D1 and N of D2
+constexpr int kMaxCluster = 8;
+constexpr int kMaxEvict = 32;      // E = L - k = b <= 32
+constexpr int kMaxTable = 128;     // n_max entries cached per request
+constexpr uint32_t kTmemCols = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+
+struct CompressArgs {
+  uint8_t* pool;
+  int64_t num_blocks;
+  const int32_t* block_tables;
+  const int32_t* dst_tables;
+  const int32_t* seq_len;
+  const int32_t* qslot;
+  float* gscores;
+  int32_t* err;
+  float* dbg_attn;
+  float* dbg_redund;
+  float* dbg_score;
+  int32_t* dbg_keep;
+  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, E, max_blocks, num_qslots;
+  float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
+  int protect_window, causal;
+};
+
+struct __align__(1024) Smem {
+  uint8_t K[2][kKeysPerCta * 128];  // [d-half][row][128 B], 128-byte swizzle
+  uint8_t Q[2][kRows * 128];
+  union {
+    float2 part[2][kRows];          // pass-1 (max, sum) per column half
+    float norm[kKeysPerCta];        // key norms (Gram diagonal)
+  } u0;
+  union {
+    float2 recv[kMaxCluster][kRows];            // (max, sum) partials of every CTA
+    struct {
+      unsigned long long key[kKeysPerCta];      // eviction keys of this CTA
+      unsigned long long wcand[kKeysPerCta];    // per-warp candidates
+    } sel;
+  } u1;
+  unsigned long long cand_recv[kMaxCluster][kMaxEvict];
+  int status_recv[kMaxCluster];
+  float row_off[kRows];
+  int evict_pos[kMaxEvict];
+  int src_tab[kMaxTable];
+  int dst_tab[kMaxTable];
+  int move_list[kKeysPerCta];       // (local key << 16) | destination slot
+  int warp_count[kThreads / 32];
+  uint64_t bar_tma;
+  uint64_t bar_mma;
+  uint32_t tmem_base;
+  int n_move;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Monotone map float -> uint32 (NaN ranks with -inf, -0 with +0).
+__device__ __forceinline__ uint32_t order_bits(float s) {
+  if (s != s) s = -INFINITY;
+  if (s == 0.0f) s = 0.0f;
+  uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Eviction key: smaller = evicted first = lower S, and on equal S the later position.
+__device__ __forceinline__ unsigned long long evict_key(float s, int t) {
+  return (static_cast<unsigned long long>(order_bits(s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(t));
+}
+
+__device__ __forceinline__ void record_error(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ size_t row_offset_bytes(const CompressArgs& a, int layer, int phys, int kv, int h,
+                                                   int row) {
+  const int64_t tile = ((static_cast<int64_t>(layer) * a.num_blocks + phys) * 2 + kv) * a.Hkv + h;
+  return static_cast<size_t>((tile * a.b + row) * a.d) * 2;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    compress_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                    const CompressArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, hh = warp >> 2;  // TMEM lane quarter, key/column half
+  const int C = static_cast<int>(cluster_nctarank());
+  const int c = static_cast<int>(cluster_ctarank());
+  const int h = blockIdx.y;
+  const int r = blockIdx.z / a.layers;
+  const int layer = blockIdx.z % a.layers;
+  const int L = a.L, b = a.b, d = a.d, w = a.w, Rw = a.Rw, Gq = a.Gq;
+  const int t0 = c * kKeysPerCta;
+  const int nk = min(kKeysPerCta, L - t0);
+  const int nhalf = d / 64;
+
+  // ---------------------------------------------------------------- set-up --------------
+  if (tid == 0) {
+    mbar_init(&s.bar_tma, 1);
+    mbar_init(&s.bar_mma, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmQ);
+  }
+  if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
+
+  // Validate the request's metadata; every CTA of the cluster sees the same values, so they
+  // all take the same decision without communicating.
+  const int slot = a.qslot[r];
+  bool bad = (a.seq_len[r] != L) || slot < 0 || slot >= a.num_qslots;
+  for (int i = tid; i < a.n_max; i += kThreads) {
+    const int sb = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + i];
+    const int db = a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + i];
+    s.src_tab[i] = sb;
+    s.dst_tab[i] = db;
+    bad |= (sb < 0 || sb >= a.num_blocks || db < 0 || db >= a.num_blocks);
+  }
+  // Zero the padding rows of Q (never touched by the TMA box).
+  for (int i = Rw * 8 + tid; i < kRows * 8; i += kThreads) {
+    const int row = i >> 3, ch = i & 7;
+    reinterpret_cast<uint4*>(s.Q[0])[row * 8 + ch] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(s.Q[1])[row * 8 + ch] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  const bool skip = __syncthreads_or(bad);
+  tc_fence_after();
+  if (skip && tid == 0 && c == 0) record_error(a.err, ZP_ERR_BAD_TABLE);
+  const uint32_t tbase = s.tmem_base;
+
+  const int kt = t0 + tid;  // the key this thread owns in passes 2..6
+  const bool key_valid = tid < nk;
+  float g_in = 0.0f;
+  int jdst = -1;  // destination slot of this thread's key if kept
+  bool fail = false;
+
+  if (!skip) {
+    if (key_valid)
+      g_in = a.gscores[((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L + kt];
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nk + Rw) * d * 2));
+      const int nblk = nk / b;
+      for (int bi = 0; bi < nblk; ++bi) {
+        const int phys = s.src_tab[t0 / b + bi];
+        for (int hd = 0; hd < nhalf; ++hd)
+          tma_load_3d(&s.K[hd][bi * b * 128], &tmK, &s.bar_tma, hd * 64, h * b,
+                      layer * static_cast<int>(a.num_blocks) + phys);
+      }
+      for (int hd = 0; hd < nhalf; ++hd)
+        tma_load_3d(&s.Q[hd][0], &tmQ, &s.bar_tma, hd * 64, h * Gq, (slot * a.layers + layer) * w);
+    }
+    fail |= !mbar_wait_bounded(&s.bar_tma, 0, kWaitNs);
+
+    // ---- D1 = Q K^T: M = 128 window rows, N = nk keys -> TMEM columns [0, nk)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, nk);
+      for (int kk = 0; kk < d / 16; ++kk) {
+        const uint64_t ad = smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32]));
+        const uint64_t bd = smem_desc_sw128(smem_u32(&s.K[kk >> 2][(kk & 3) * 32]));
+        mma_bf16(tbase, ad, bd, idesc, kk > 0);
+      }
+      mma_commit(&s.bar_mma);
+    }
+    fail |= !mbar_wait_bounded(&s.bar_mma, 0, kWaitNs);
+    tc_fence_after();
+
+    // ---- pass 1: per-row max and exp-sum over this CTA's keys (thread = row, half of columns)
+    {
+      const int i = q4 * 32 + lane;
+      const bool row_ok = i < Rw;
+      const int t_lim = a.causal ? (L - w + i / Gq) : (L - 1);
+      float m = -INFINITY;
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int col0 = hh * 128 + c4 * 32;
+        if (col0 >= nk) break;
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + col0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const bool ok = row_ok && (col0 + j < nk) && (t0 + col0 + j <= t_lim);
+          if (ok) m = fmaxf(m, v[j]);
+        }
+      }
+      // second sweep: every lane runs the same collective loads; rows without a visible key
+      // never pass the predicate, so their -inf maximum is never used
+      float l = 0.0f;
+      const float mo = m * a.sl2;
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int col0 = hh * 128 + c4 * 32;
+        if (col0 >= nk) break;
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + col0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const bool ok = row_ok && (col0 + j < nk) && (t0 + col0 + j <= t_lim);
+          if (ok) l += ex2(fmaf(v[j], a.sl2, -mo));
+        }
+      }
+      s.u0.part[hh][i] = make_float2(m, l);
+    }
+  }
+  tc_fence_before();
+  fail = __syncthreads_or(fail);
+  tc_fence_after();
+
+  if (!skip) {
+    // Gram of each 128-key half: TMEM columns [128*kh, 128*kh + 128); D1 is fully read.
+    if (tid == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 128);
+      for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
+        for (int kk = 0; kk < d / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32]));
+          mma_bf16(tbase + kh * 128, ad, ad, idesc, kk > 0);
+        }
+      mma_commit(&s.bar_mma);
+    }
+    // merge the two column halves and push (max, sum) of each row to every CTA
+    if (tid < kRows) {
+      const float2 p0 = s.u0.part[0][tid], p1 = s.u0.part[1][tid];
+      float m = fmaxf(p0.x, p1.x), l = 0.0f;
+      if (m != -INFINITY) {
+        if (p0.y > 0.0f) l += p0.y * ex2((p0.x - m) * a.sl2);
+        if (p1.y > 0.0f) l += p1.y * ex2((p1.x - m) * a.sl2);
+      }
+      const uint32_t local = smem_u32(&s.u1.recv[c][tid]);
+      for (int dst = 0; dst < C; ++dst) st_cluster_v2(mapa(local, dst), m, l);
+    }
+  }
+  cluster_sync();  // #1: every CTA's row partials have landed
+
+  float attn = 0.0f, red = 0.0f, S = 0.0f;
+  if (!skip) {
+    if (tid < kRows) {
+      float M = -INFINITY;
+      for (int cc = 0; cc < C; ++cc) M = fmaxf(M, s.u1.recv[cc][tid].x);
+      float Lsum = 0.0f;
+      if (M != -INFINITY)
+        for (int cc = 0; cc < C; ++cc) {
+          const float2 p = s.u1.recv[cc][tid];
+          if (p.y > 0.0f) Lsum += p.y * ex2((p.x - M) * a.sl2);
+        }
+      s.row_off[tid] = (tid < Rw && Lsum > 0.0f) ? fmaf(M, a.sl2, lg2(Lsum)) : INFINITY;
+    }
+
+    // ---- Lightning redundancy from the Gram (thread = key)
+    fail |= !mbar_wait_bounded(&s.bar_mma, 1, kWaitNs);
+    tc_fence_after();
+    float gv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) gv[j] = 0.0f;
+    const int wcol = hh * 128 + q4 * 32;  // first key (and Gram column) of this warp
+    if (wcol < nk) tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + wcol, gv);
+    float diag = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j == lane) diag = gv[j];
+    s.u0.norm[tid] = fmaxf(sqrtf(fmaxf(diag, 0.0f)), 1e-12f);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // D2 = K Q^T per 128-key half into the same TMEM columns (Gram fully read)
+    if (tid == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 128);
+      for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
+        for (int kk = 0; kk < d / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32]));
+          const uint64_t bd = smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32]));
+          mma_bf16(tbase + kh * 128, ad, bd, idesc, kk > 0);
+        }
+      mma_commit(&s.bar_mma);
+    }
+    if (key_valid) {
+      const int jb0 = (tid % 32) / b * b;  // first column of this key's block within gv
+      const float nt = s.u0.norm[tid];
+      float acc = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j >= jb0 && j < jb0 + b && j != lane) acc += gv[j] / (nt * s.u0.norm[(tid & ~31) + j]);
+      red = acc / static_cast<float>(b - 1);
+    }
+
+    // ---- pass 2: attention mass of this key over the window rows
+    fail |= !mbar_wait_bounded(&s.bar_mma, 0, kWaitNs);
+    tc_fence_after();
+    if (wcol < nk) {
+      const int imin = a.causal ? max(0, Gq * (kt - (L - w))) : 0;
+      float acc = 0.0f;
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128 + c4 * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int i = c4 * 32 + j;
+          if (i >= imin) acc += ex2(fmaf(v[j], a.sl2, -s.row_off[i]));
+        }
+      }
+      attn = acc / static_cast<float>(Rw);
+    }
+    S = (attn + a.alpha * g_in) - a.beta * red;
+    if (a.protect_window && kt >= L - w) S = INFINITY;
+
+    if (key_valid) {
+      const int64_t o = ((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt;
+      if (a.dbg_attn) a.dbg_attn[o] = attn;
+      if (a.dbg_redund) a.dbg_redund[o] = red;
+      if (a.dbg_score) a.dbg_score[o] = S;
+    }
+
+    // ---- selection, level 1: per-warp bottom-E by rank counting over the warp's 32 keys
+    const int E = a.E;
+    const unsigned long long mykey = key_valid ? evict_key(S, kt) : (~0ull - static_cast<unsigned long long>(tid));
+    int wr = 0;
+#pragma unroll 8
+    for (int u = 0; u < 32; ++u) wr += (__shfl_sync(0xffffffffu, mykey, u) < mykey) ? 1 : 0;
+    const int wE = min(E, 32);
+    if (wr < wE) s.u1.sel.wcand[warp * wE + wr] = mykey;
+  }
+  tc_fence_before();
+  fail = __syncthreads_or(fail);
+  tc_fence_after();
+
+  if (!skip) {
+    // level 2: rank each warp candidate among all of this CTA's warp candidates
+    const int E = a.E;
+    const int ncand = (kThreads / 32) * min(E, 32);
+    if (tid < ncand) {
+      const unsigned long long key = s.u1.sel.wcand[tid];
+      int rk = 0;
+      for (int u = 0; u < ncand; ++u) rk += (s.u1.sel.wcand[u] < key) ? 1 : 0;
+      if (rk < E) {
+        const uint32_t local = smem_u32(&s.cand_recv[c][rk]);
+        for (int dst = 0; dst < C; ++dst) st_cluster_u64(mapa(local, dst), key);
+      }
+    }
+    if (tid == 0) {
+      const uint32_t local = smem_u32(&s.status_recv[c]);
+      for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), fail ? 1u : 0u);
+    }
+  }
+  cluster_sync();  // #2: candidates and statuses of every CTA have landed
+
+  bool any_fail = false;
+  if (!skip) {
+    for (int cc = 0; cc < C; ++cc) any_fail |= s.status_recv[cc] != 0;
+    const int E = a.E;
+    const int ntot = C * E;
+    // level 3: the E lowest keys of the cluster, identical in every CTA
+    if (tid < ntot) {
+      const unsigned long long key = s.cand_recv[tid / E][tid % E];
+      int rk = 0;
+      for (int u = 0; u < ntot; ++u) rk += (s.cand_recv[u / E][u % E] < key) ? 1 : 0;
+      if (rk < E) s.evict_pos[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
+    }
+    __syncthreads();
+
+    // destination of this CTA's keys: j = t - #(evicted before t)
+    bool evicted = false, moved = false;
+    int j = 0;
+    if (key_valid) {
+      int shift = 0;
+      for (int e = 0; e < E; ++e) {
+        const int p = s.evict_pos[e];
+        shift += (p < kt) ? 1 : 0;
+        evicted |= (p == kt);
+      }
+      j = kt - shift;
+      if (!evicted) {
+        const int sp = s.src_tab[kt / b], dp = s.dst_tab[j / b];
+        moved = (sp != dp) || (kt % b != j % b);
+      }
+      if (a.dbg_keep)
+        a.dbg_keep[((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt] = evicted ? 0 : 1;
+    }
+    // compact list of moved keys (warp ballot + scan over the 8 warps)
+    const unsigned ball = __ballot_sync(0xffffffffu, moved);
+    if (lane == 0) s.warp_count[warp] = __popc(ball);
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int ww = 0; ww < kThreads / 32; ++ww) {
+      base += (ww < warp) ? s.warp_count[ww] : 0;
+      total += s.warp_count[ww];
+    }
+    if (moved) s.move_list[base + __popc(ball & ((1u << lane) - 1))] = (tid << 16) | j;
+    if (tid == 0) s.n_move = total;
+    __syncthreads();
+
+    // global-score update of kept keys; written after the barrier
+    if (key_valid && !evicted) {
+      g_in = a.decay * g_in + attn;
+      jdst = j;
+    }
+  }
+
+  // ---- V rows that move: into registers before the barrier (warp w owns list entries
+  //      [32w, 32w+32); cpr 16-byte chunks per row, rpi rows per warp iteration)
+  const int cpr = d / 8, rpi = 32 / cpr, iters = 32 / rpi;
+  uint4 vbuf[16];
+  if (!skip) {
+    const int n_move = s.n_move;
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int e = warp * 32 + it * rpi + lane / cpr, ch = lane % cpr;
+      vbuf[it] = make_uint4(0, 0, 0, 0);
+      if (it < iters && e < n_move) {
+        const int kl = s.move_list[e] >> 16;
+        const int t = t0 + kl;
+        const uint8_t* src = a.pool + row_offset_bytes(a, layer, s.src_tab[t / b], 1, h, t % b) + ch * 16;
+        vbuf[it] = *reinterpret_cast<const uint4*>(src);
+      }
+    }
+  }
+  cluster_sync();  // #3: every read of the unit (K by TMA, V, G) precedes every write
+
+  if (!skip && !any_fail) {
+    const int n_move = s.n_move;
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int e = warp * 32 + it * rpi + lane / cpr, ch = lane % cpr;
+      if (it < iters && e < n_move) {
+        const int packed = s.move_list[e];
+        const int kl = packed >> 16, jj = packed & 0xFFFF;
+        const int dp = s.dst_tab[jj / b];
+        const int half = ch >> 3, c8 = ch & 7;
+        const uint4 kv = *reinterpret_cast<const uint4*>(&s.K[half][kl * 128 + ((c8 ^ (kl & 7)) << 4)]);
+        uint8_t* dk = a.pool + row_offset_bytes(a, layer, dp, 0, h, jj % b) + ch * 16;
+        uint8_t* dv = a.pool + row_offset_bytes(a, layer, dp, 1, h, jj % b) + ch * 16;
+        *reinterpret_cast<uint4*>(dk) = kv;
+        *reinterpret_cast<uint4*>(dv) = vbuf[it];
+      }
+    }
+    float* G = a.gscores + ((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L;
+    if (jdst >= 0) G[jdst] = g_in;
+    if (c == C - 1 && tid < a.E) G[a.k + tid] = 0.0f;
+  }
+  if (!skip && any_fail && tid == 0 && c == 0) record_error(a.err, ZP_ERR_TIMEOUT);
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+}  // namespace
+
+size_t compress_smem_bytes() { return sizeof(Smem) + 1024; }
+
+}  // namespace zp
+
+using namespace zp;
+
+extern "C" size_t zp_compress_workspace_size(const zp_params*, int32_t) { return 256; }
+
+extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
+                                 const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
+                                 const zp_params* p, const zp_debug* dbg, void* workspace,
+                                 size_t workspace_bytes, zp_stream stream) {
+  if (!pool || !meta || !obs_q || !global_scores || !p || !workspace) return ZP_ERR_INVALID_ARG;
+  if (!pool->base || pool->num_blocks <= 0) return ZP_ERR_INVALID_ARG;
+  // with no request the per-request arrays may be empty (NULL)
+  if (meta->num_requests > 0 && (!block_tables || !meta->seq_len || !meta->qslot || !meta->dst_tables))
+    return ZP_ERR_INVALID_ARG;
+  if (workspace_bytes < zp_compress_workspace_size(p, meta->num_requests) || !aligned(workspace, 256))
+    return ZP_ERR_INVALID_ARG;
+  const int layers = p->num_layers, Hq = p->num_q_heads, Hkv = p->num_kv_heads, d = p->head_dim,
+            b = p->block_size, n_max = p->n_max, w = p->window, R = meta->num_requests;
+  if (layers <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || R < 0 || num_qslots <= 0) return ZP_ERR_INVALID_ARG;
+  if (n_max < 2 || meta->max_blocks < n_max || w < 1) return ZP_ERR_INVALID_ARG;
+  const int L = n_max * b, k = (n_max - 1) * b, Gq = Hq / Hkv, Rw = w * Gq;
+  if (w > k) return ZP_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ZP_ERR_UNSUPPORTED;
+  if (b != 16 && b != 32) return ZP_ERR_UNSUPPORTED;
+  if (Rw > kRows || n_max > kMaxTable || (L + kKeysPerCta - 1) / kKeysPerCta > kMaxCluster)
+    return ZP_ERR_UNSUPPORTED;
+  if (Gq > 256 || w > 256) return ZP_ERR_UNSUPPORTED;
+  if (!aligned(pool->base, 16) || !aligned(obs_q, 16)) return ZP_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(layers) * pool->num_blocks >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(R) * layers > 65535) return ZP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_qslots) * layers * w >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 4, st) != cudaSuccess) return ZP_ERR_CUDA;
+  if (R == 0) return ZP_OK;
+
+  CUtensorMap tmK, tmQ;
+  // K/V pool as {d, 2*Hkv*b rows per (layer, block), layers*num_blocks}; box = one block's
+  // b rows of one head, 64 columns.
+  if (!encode_tmap_3d_bf16(&tmK, pool->base, d, static_cast<uint64_t>(2) * Hkv * b,
+                           static_cast<uint64_t>(layers) * pool->num_blocks, static_cast<uint64_t>(d) * 2,
+                           static_cast<uint64_t>(2) * Hkv * b * d * 2, 64, b, 1))
+    return ZP_ERR_CUDA;
+  // window queries as {d, Hq, slots*layers*w}; box = the G_q heads of one kv head x w rows.
+  if (!encode_tmap_3d_bf16(&tmQ, obs_q, d, Hq, static_cast<uint64_t>(num_qslots) * layers * w,
+                           static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(Hq) * d * 2, 64, Gq, w))
+    return ZP_ERR_CUDA;
+
+  CompressArgs a{};
+  a.pool = static_cast<uint8_t*>(pool->base);
+  a.num_blocks = pool->num_blocks;
+  a.block_tables = block_tables;
+  a.dst_tables = meta->dst_tables;
+  a.seq_len = meta->seq_len;
+  a.qslot = meta->qslot;
+  a.gscores = global_scores;
+  a.err = static_cast<int32_t*>(workspace);
+  if (dbg) {
+    a.dbg_attn = dbg->attn;
+    a.dbg_redund = dbg->redund;
+    a.dbg_score = dbg->score;
+    a.dbg_keep = dbg->keep;
+  }
+  a.R = R;
+  a.layers = layers;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.b = b;
+  a.n_max = n_max;
+  a.w = w;
+  a.Gq = Gq;
+  a.Rw = Rw;
+  a.L = L;
+  a.k = k;
+  a.E = L - k;
+  a.max_blocks = meta->max_blocks;
+  a.num_qslots = num_qslots;
+  a.alpha = p->alpha;
+  a.beta = p->beta;
+  a.decay = p->decay;
+  a.sl2 = p->scale * 1.4426950408889634f;
+  a.protect_window = p->protect_window;
+  a.causal = p->causal;
+
+  const size_t smem = compress_smem_bytes();
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+  });
+  if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
+
+  const int C = (L + kKeysPerCta - 1) / kKeysPerCta;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(C, Hkv, R * layers);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, compress_kernel, tmK, tmQ, a) != cudaSuccess) return ZP_ERR_CUDA;
+  return ZP_OK;
+}

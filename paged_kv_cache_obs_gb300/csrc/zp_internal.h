@@ -1,0 +1,24 @@
+// zp_internal.h — host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/zipage.h"
+
+namespace zp {
+
+// Encodes a 3-D bf16 tiled tensor map with 128-byte swizzle.  dims/strides in elements/bytes
+// (strides of dims 1 and 2), box in elements.  Returns false if the driver rejects it.
+bool encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                         uint32_t box2);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace zp

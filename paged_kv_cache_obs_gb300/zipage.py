@@ -1,0 +1,267 @@
+"""ctypes binding of libzipage.so — argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/zipage.h) and does
+nothing but turn tensors into pointers, fill the C structs and raise on a non-OK status.  All
+computation of the compression pass and of decode attention runs in the library's CUDA
+kernels; there is no fallback: if the library is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libzipage.so")
+
+ZP_OK = 0
+ZP_ERR_INVALID_ARG = 1
+ZP_ERR_NO_BLOCKS = 2
+ZP_ERR_BAD_TABLE = 3
+ZP_ERR_TIMEOUT = 4
+ZP_ERR_CUDA = 5
+ZP_ERR_UNSUPPORTED = 6
+_NAMES = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_NO_BLOCKS", 3: "ZP_ERR_BAD_TABLE",
+          4: "ZP_ERR_TIMEOUT", 5: "ZP_ERR_CUDA", 6: "ZP_ERR_UNSUPPORTED"}
+
+
+class ZipageError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} returned {_NAMES.get(status, status)}")
+        self.status = status
+
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libzipage.so is not built ({_LIB_PATH}); run __graft_entry__.build() "
+                      "or python -m paged_kv_cache_obs_gb300.build")
+lib = ctypes.CDLL(_LIB_PATH)
+
+
+class zp_params(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("n_max", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("decay", ctypes.c_float),
+                ("scale", ctypes.c_float), ("protect_window", ctypes.c_int32),
+                ("causal", ctypes.c_int32)]
+
+
+class zp_kv_pool(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64)]
+
+
+class zp_seq_meta(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("seq_len", ctypes.c_void_p), ("qslot", ctypes.c_void_p),
+                ("dst_tables", ctypes.c_void_p)]
+
+
+class zp_debug(ctypes.Structure):
+    _fields_ = [("attn", ctypes.c_void_p), ("redund", ctypes.c_void_p),
+                ("score", ctypes.c_void_p), ("keep", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def _sig(name, res, args):
+    f = getattr(lib, name)
+    f.restype = res
+    f.argtypes = args
+    return f
+
+
+_sig("zp_compress", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta), _P, _I32, _P,
+                           ctypes.POINTER(zp_params), ctypes.POINTER(zp_debug), _P, _SZ, _P])
+_sig("zp_compress_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32])
+_sig("zp_paged_decode_attn", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
+                                    ctypes.POINTER(zp_params), _P, _SZ, _P])
+_sig("zp_paged_decode_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
+_sig("zp_read_error", _I32, [_P, _P, _I32P])
+_sig("zp_alloc_create", _I32, [_I64, ctypes.POINTER(_P)])
+_sig("zp_alloc_destroy", None, [_P])
+_sig("zp_alloc_blocks", _I32, [_P, _I32, _P])
+_sig("zp_alloc_reserve", _I32, [_P, _P, _I32])
+_sig("zp_incref", _I32, [_P, _P, _I32])
+_sig("zp_decref", _I32, [_P, _P, _I32])
+_sig("zp_decref_after", _I32, [_P, _P, _I32, _P])
+_sig("zp_alloc_poll", _I32, [_P])
+_sig("zp_alloc_drain", _I32, [_P])
+_sig("zp_alloc_inject_failure", _I32, [_P, _I64])
+_sig("zp_refcount", _I32, [_P, _I32])
+_sig("zp_num_free", _I64, [_P])
+_sig("zp_num_pending", _I64, [_P])
+_sig("zp_plan_compress", _I32, [_P, _P, _I32, _I32, _I32, _P])
+_sig("zp_commit_compress", _I32, [_P, _P, _P, _I32, _I32, _I32, _P])
+_sig("zp_version", _I32, [])
+
+
+def _check(fn, status):
+    if status != ZP_OK:
+        raise ZipageError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_params(p: dict) -> zp_params:
+    return zp_params(p["num_layers"], p["num_q_heads"], p["num_kv_heads"], p["head_dim"],
+                     p["block_size"], p["n_max"], p["window"], p["alpha"], p["beta"], p["decay"],
+                     p["scale"], int(p["protect_window"]), int(p["causal"]))
+
+
+def _i32_array(a):
+    """Contiguous host int32 buffer (numpy array or sequence) -> (ctypes array, keepalive)."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return arr.ctypes.data_as(ctypes.c_void_p), arr
+
+
+# ------------------------------------------------------------------ compression pass --------
+
+def zp_compress_workspace_size(params: dict, num_requests: int) -> int:
+    return lib.zp_compress_workspace_size(ctypes.byref(make_params(params)), num_requests)
+
+
+def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_scores, params: dict,
+                workspace, debug: dict | None = None, stream=None):
+    """Queues the compression pass; tensors are device tensors (see include/zipage.h)."""
+    kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    meta = zp_seq_meta(block_tables.shape[0], block_tables.shape[1], seq_len.data_ptr(),
+                       qslot.data_ptr(), dst_tables.data_ptr())
+    dbg = None
+    if debug:
+        dbg = zp_debug(*(debug[k].data_ptr() if debug.get(k) is not None else None
+                         for k in ("attn", "redund", "score", "keep")))
+    st = lib.zp_compress(ctypes.byref(kv), _ptr(block_tables), ctypes.byref(meta), _ptr(obs_q),
+                         obs_q.shape[0], _ptr(global_scores), ctypes.byref(make_params(params)),
+                         ctypes.byref(dbg) if dbg is not None else None, _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("zp_compress", st)
+
+
+# ------------------------------------------------------------------ decode attention ---------
+
+def zp_paged_decode_workspace_size(params: dict, B: int, max_blocks: int) -> int:
+    return lib.zp_paged_decode_workspace_size(ctypes.byref(make_params(params)), B, max_blocks)
+
+
+def zp_paged_decode_attn(pool, layer: int, q, block_tables, seq_lens, out, params: dict, workspace,
+                         stream=None):
+    kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    st = lib.zp_paged_decode_attn(ctypes.byref(kv), layer, _ptr(q), _ptr(block_tables), _ptr(seq_lens),
+                                  q.shape[0], block_tables.shape[1], _ptr(out),
+                                  ctypes.byref(make_params(params)), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("zp_paged_decode_attn", st)
+
+
+def zp_read_error(workspace, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check("zp_read_error", lib.zp_read_error(_ptr(workspace), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def new_workspace(nbytes: int, device="cuda"):
+    """Device workspace of at least nbytes (256-byte aligned: torch allocations are)."""
+    return torch.zeros(max(256, (nbytes + 255) // 256 * 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ allocator (host) --------
+
+def zp_alloc_create(num_blocks: int):
+    h = ctypes.c_void_p()
+    _check("zp_alloc_create", lib.zp_alloc_create(num_blocks, ctypes.byref(h)))
+    return h
+
+
+def zp_alloc_destroy(a):
+    lib.zp_alloc_destroy(a)
+
+
+def zp_alloc_blocks(a, n: int):
+    import numpy as np
+    ids = np.zeros(max(n, 1), dtype=np.int32)
+    _check("zp_alloc_blocks", lib.zp_alloc_blocks(a, n, ids.ctypes.data_as(ctypes.c_void_p)))
+    return ids[:n]
+
+
+def zp_alloc_reserve(a, ids):
+    p, keep = _i32_array(ids)
+    _check("zp_alloc_reserve", lib.zp_alloc_reserve(a, p, len(keep)))
+
+
+def zp_incref(a, ids):
+    p, keep = _i32_array(ids)
+    _check("zp_incref", lib.zp_incref(a, p, len(keep)))
+
+
+def zp_decref(a, ids):
+    p, keep = _i32_array(ids)
+    _check("zp_decref", lib.zp_decref(a, p, len(keep)))
+
+
+def zp_decref_after(a, ids, stream=None):
+    p, keep = _i32_array(ids)
+    st = None if stream is False else _stream(stream)
+    _check("zp_decref_after", lib.zp_decref_after(a, p, len(keep), st))
+
+
+def zp_alloc_poll(a):
+    _check("zp_alloc_poll", lib.zp_alloc_poll(a))
+
+
+def zp_alloc_drain(a):
+    _check("zp_alloc_drain", lib.zp_alloc_drain(a))
+
+
+def zp_alloc_inject_failure(a, nth_call: int):
+    _check("zp_alloc_inject_failure", lib.zp_alloc_inject_failure(a, nth_call))
+
+
+def zp_refcount(a, block_id: int) -> int:
+    return lib.zp_refcount(a, block_id)
+
+
+def zp_num_free(a) -> int:
+    return lib.zp_num_free(a)
+
+
+def zp_num_pending(a) -> int:
+    return lib.zp_num_pending(a)
+
+
+def zp_plan_compress(a, host_tables, n_max: int):
+    """host_tables: int32 [R, max_blocks] (numpy) -> destination tables (numpy)."""
+    import numpy as np
+    t = np.ascontiguousarray(host_tables, dtype=np.int32)
+    out = np.zeros_like(t)
+    _check("zp_plan_compress", lib.zp_plan_compress(a, t.ctypes.data_as(ctypes.c_void_p), t.shape[0],
+                                                    t.shape[1], n_max,
+                                                    out.ctypes.data_as(ctypes.c_void_p)))
+    return out
+
+
+def zp_commit_compress(a, old_tables, new_tables, n_max: int, stream=None):
+    import numpy as np
+    o = np.ascontiguousarray(old_tables, dtype=np.int32)
+    n = np.ascontiguousarray(new_tables, dtype=np.int32)
+    st = None if stream is False else _stream(stream)
+    _check("zp_commit_compress", lib.zp_commit_compress(a, o.ctypes.data_as(ctypes.c_void_p),
+                                                        n.ctypes.data_as(ctypes.c_void_p), o.shape[0],
+                                                        o.shape[1], n_max, st))
+
+
+def zp_version() -> int:
+    return lib.zp_version()

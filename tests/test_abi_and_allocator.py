@@ -1,0 +1,159 @@
+"""C-ABI library: it loads, exports every entry point of include/zipage.h, and its host-side
+allocator / planner behave like the literal refcount model (no GPU needed for any of this)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import zipage_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def zp():
+    from paged_kv_cache_obs_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from paged_kv_cache_obs_gb300 import zipage
+    return zipage
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(zp_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(zp):
+    names = _declared_symbols()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(zp.lib, n), n
+    assert zp.zp_version() == 1
+
+
+def test_alloc_lowest_first_and_transactional(zp):
+    a = zp.zp_alloc_create(8)
+    try:
+        assert list(zp.zp_alloc_blocks(a, 3)) == [0, 1, 2]
+        assert zp.zp_num_free(a) == 5
+        with pytest.raises(zp.ZipageError) as e:
+            zp.zp_alloc_blocks(a, 6)
+        assert e.value.status == zp.ZP_ERR_NO_BLOCKS
+        assert zp.zp_num_free(a) == 5            # nothing changed
+        zp.zp_decref(a, [1])
+        assert zp.zp_refcount(a, 1) == 0
+        assert list(zp.zp_alloc_blocks(a, 2)) == [1, 3]
+        with pytest.raises(zp.ZipageError):
+            zp.zp_decref(a, [5])                  # free block
+        with pytest.raises(zp.ZipageError):
+            zp.zp_decref(a, [0, 0])               # refcount 1, two decrefs: all-or-nothing
+        assert zp.zp_refcount(a, 0) == 1
+        assert zp.zp_refcount(a, 99) == -1
+    finally:
+        zp.zp_alloc_destroy(a)
+
+
+def test_reserve_incref_and_injected_failure(zp):
+    a = zp.zp_alloc_create(10)
+    try:
+        zp.zp_alloc_reserve(a, [7, 2, 5])
+        assert [zp.zp_refcount(a, i) for i in (2, 5, 7)] == [1, 1, 1]
+        with pytest.raises(zp.ZipageError):
+            zp.zp_alloc_reserve(a, [3, 3])
+        with pytest.raises(zp.ZipageError):
+            zp.zp_alloc_reserve(a, [2])
+        zp.zp_incref(a, [5, 5])
+        assert zp.zp_refcount(a, 5) == 3
+        zp.zp_alloc_inject_failure(a, 2)
+        zp.zp_alloc_blocks(a, 1)                   # first call succeeds
+        free_before = zp.zp_num_free(a)
+        with pytest.raises(zp.ZipageError) as e:
+            zp.zp_alloc_blocks(a, 1)               # second fails, changes nothing
+        assert e.value.status == zp.ZP_ERR_NO_BLOCKS and zp.zp_num_free(a) == free_before
+        zp.zp_alloc_blocks(a, 1)
+    finally:
+        zp.zp_alloc_destroy(a)
+
+
+def _state_from(inp_refcount):
+    return {i: int(c) for i, c in enumerate(inp_refcount)}
+
+
+@pytest.mark.parametrize("prefix", [0, 4])
+def test_plan_and_commit_match_refcount_model(zp, prefix):
+    rng = np.random.default_rng(prefix)
+    NB, R, n_max, mb = 200, 5, 12, 14
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((R, mb), -1, np.int32)
+    shared = perm[:prefix]
+    nxt = prefix
+    for r in range(R):
+        tables[r, :prefix] = shared
+        tables[r, prefix:n_max] = perm[nxt:nxt + n_max - prefix]
+        nxt += n_max - prefix
+    model = O.RefcountPool(NB)
+    a = zp.zp_alloc_create(NB)
+    try:
+        used = sorted(set(tables[tables >= 0].tolist()))
+        zp.zp_alloc_reserve(a, used)
+        for i in used:
+            model.refcount[i] = 1
+        if prefix:
+            extra = list(shared) * R  # R requests + the prefix cache's own reference
+            zp.zp_incref(a, extra)
+            model.incref(extra)
+        dst = zp.zp_plan_compress(a, tables, n_max)
+        free = model.free_ids()
+        want = tables.copy()
+        for r in range(R):
+            row, _ = O.plan_dst_table(tables[r], n_max, dict(enumerate(model.refcount)), free)
+            want[r, :n_max - 1] = row
+        fresh = want[:, :prefix].ravel().tolist()
+        for i in fresh:
+            model.refcount[i] = 1
+        assert np.array_equal(dst, want)
+        assert zp.zp_num_free(a) == model.num_free()
+        # commit, deferred only by a NULL stream here (host-only): released at once
+        zp.zp_commit_compress(a, tables, dst, n_max, stream=False)
+        for r in range(R):
+            rel = [tables[r, i] for i in range(n_max - 1) if tables[r, i] != dst[r, i]] + [tables[r, n_max - 1]]
+            model.decref(rel)
+        assert [zp.zp_refcount(a, i) for i in range(NB)] == model.refcount
+        # one freed last block per request; shared blocks stay live (prefix-cache reference)
+        assert zp.zp_num_free(a) == NB - (R * (n_max - 1) + (prefix and prefix))
+        for s in shared:
+            assert zp.zp_refcount(a, int(s)) == 1
+        # the planner is transactional when blocks run out
+        if prefix:
+            with pytest.raises(zp.ZipageError):
+                zp.zp_incref(a, [999])
+            big = dst[:1].copy()
+            big[0, n_max - 1] = zp.zp_alloc_blocks(a, 1)[0]   # a new last block
+            zp.zp_incref(a, list(big[0, :n_max - 1]))          # make request 0's blocks shared
+            zp.zp_alloc_inject_failure(a, 1)
+            before = [zp.zp_refcount(a, i) for i in range(NB)]
+            with pytest.raises(zp.ZipageError) as e:
+                zp.zp_plan_compress(a, big, n_max)
+            assert e.value.status == zp.ZP_ERR_NO_BLOCKS
+            assert [zp.zp_refcount(a, i) for i in range(NB)] == before
+    finally:
+        zp.zp_alloc_destroy(a)
+
+
+def test_invalid_arguments_are_rejected_without_a_gpu(zp):
+    p = dict(num_layers=1, num_q_heads=4, num_kv_heads=3, head_dim=64, block_size=16, n_max=8,
+             window=8, alpha=0.5, beta=0.5, decay=0.9, scale=0.125, protect_window=1, causal=1)
+    import ctypes
+    kv = zp.zp_kv_pool(None, 0)
+    st = zp.lib.zp_compress(ctypes.byref(kv), None, None, None, 1, None,
+                            ctypes.byref(zp.make_params(p)), None, None, 0, None)
+    assert st == zp.ZP_ERR_INVALID_ARG
+    assert zp.zp_compress_workspace_size(p, 4) >= 4
+    assert zp.zp_paged_decode_workspace_size(dict(p, num_kv_heads=2), 3, 20) > 256

@@ -1,0 +1,234 @@
+"""GPU parity of the compression pass (C-ABI zp_compress) against the CPU oracle.
+
+Small cases compare every unit and every byte of the pool; the full-size workloads run in
+the launch configuration the benchmark times and compare sampled units with the oracle plus
+size-independent properties of all units.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import parity
+from oracle import zipage_oracle as O
+from paged_kv_cache_obs_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zp():
+    from paged_kv_cache_obs_gb300 import build
+    import os
+    if not os.path.exists(build.LIB):
+        build.build()
+    from paged_kv_cache_obs_gb300 import runner, zipage
+    return zipage, runner
+
+
+def _run(zp, wl, device_gen=False, seed=None, mutate=None):
+    zipage, runner = zp
+    inp = synth.make_inputs(wl, "cuda" if device_gen else "cpu", seed=seed)
+    if mutate:
+        mutate(inp)
+    pool_in = synth.bf16_bits(inp.pool)
+    obs_q = synth.bf16_bits(inp.obs_q)
+    gs_in = inp.global_scores.cpu().numpy()
+    batch = runner.CompressionBatch(inp, "cuda")
+    batch.enable_debug()
+    batch.launch()
+    err = batch.error()
+    torch.cuda.synchronize()
+    return inp, batch, pool_in, obs_q, gs_in, err
+
+
+def _check_all(zp, wl, **kw):
+    inp, batch, pool_in, obs_q, gs_in, err = _run(zp, wl, **kw)
+    assert err == 0
+    R = inp.num_compress
+    units = [(r, l, h) for r in range(R) for l in range(wl.num_layers) for h in range(wl.num_kv_heads)]
+    dbg = {k: v.cpu().numpy() for k, v in batch.debug.items()}
+    ndiff = parity.check_units(units, pool_in, obs_q, gs_in, batch.tables, batch.dst_tables,
+                               inp.seq_len[:R], inp.qslot, wl.params(), dbg,
+                               batch.gs.cpu().numpy(), synth.bf16_bits(batch.pool), full_pool=True)
+    batch.close()
+    return ndiff
+
+
+SMALL = {
+    "tiny": synth.WORKLOADS["tiny"],
+    "qwen2_small": synth.WORKLOADS["qwen2_7b"].scaled(num_requests=2, num_layers=2),
+    "llama3_small": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2),
+    "prefix_small": synth.WORKLOADS["shared_prefix"].scaled(num_requests=3, num_layers=2),
+    # L = 1152: five CTAs, the last one holds a ragged 128 keys
+    "ragged_cluster": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, n_max=72),
+    # L = 144: one CTA whose second key half holds 16 keys
+    "ragged_cta": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, n_max=9, window=8),
+    # d = 64 with b = 32 and L = 320: two CTAs, 64 keys in the second
+    "d64_b32": synth.WORKLOADS["tiny"].scaled(num_requests=2, num_layers=2, num_q_heads=8,
+                                              num_kv_heads=2, block_size=32, n_max=10, window=4,
+                                              global_init="uniform"),
+    "no_protect_noncausal": synth.WORKLOADS["llama3_8b"].scaled(num_requests=1, num_layers=2, n_max=16,
+                                                                protect_window=0, causal=0),
+    "one_window_row": synth.WORKLOADS["qwen2_7b"].scaled(num_requests=1, num_layers=1, n_max=8, window=1),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_compress_matches_oracle_every_unit(zp, name):
+    ndiff = _check_all(zp, SMALL[name])
+    assert ndiff <= 2
+
+
+def test_exact_ties_keep_the_earlier_tokens(zp):
+    # all keys of a head identical, no global score, alpha = beta = 0, non-causal: every
+    # unprotected token has the same score, so the earliest k tokens are kept.
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=1, num_layers=1, n_max=24, alpha=0.0,
+                                             beta=0.0, causal=0, protect_window=0)
+
+    def mutate(inp):
+        inp.pool[:, :, 0] = inp.pool[:, :1, 0, :, :1]
+
+    inp, batch, pool_in, obs_q, gs_in, err = _run(zp, wl, mutate=mutate)
+    assert err == 0
+    k = (wl.n_max - 1) * wl.block_size
+    keep = batch.debug["keep"].cpu().numpy()[0, 0]
+    for h in range(wl.num_kv_heads):
+        assert np.array_equal(np.nonzero(keep[h])[0], np.arange(k))
+    batch.close()
+
+
+def test_bad_block_id_skips_the_request_and_reports(zp):
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, n_max=16)
+    zipage, runner = zp
+    inp = synth.make_inputs(wl, "cpu")
+    pool_in = synth.bf16_bits(inp.pool)
+    batch = runner.CompressionBatch(inp, "cuda")
+    bad = batch.d_tables.clone()
+    bad[1, 3] = inp.pool.shape[1] + 5  # request 1 points outside the pool
+    batch.d_tables = bad
+    batch.launch()
+    assert batch.error() == zipage.ZP_ERR_BAD_TABLE
+    out = synth.bf16_bits(batch.pool)
+    # request 1's blocks are untouched; request 0 was compressed
+    for blk in inp.block_tables[1, :wl.n_max]:
+        assert np.array_equal(out[:, blk], pool_in[:, blk])
+    assert not np.array_equal(out[:, inp.block_tables[0, :wl.n_max - 1]],
+                              pool_in[:, inp.block_tables[0, :wl.n_max - 1]])
+    batch.close()
+
+
+def test_unsupported_and_empty_calls(zp):
+    zipage, runner = zp
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=1, num_layers=1, n_max=8)
+    inp = synth.make_inputs(wl, "cpu")
+    batch = runner.CompressionBatch(inp, "cuda")
+    with pytest.raises(zipage.ZipageError) as e:   # L = 160*16 > 2048 keys per unit
+        zipage.zp_compress(batch.pool, batch.d_tables, batch.d_seq, batch.d_qslot, batch.d_dst,
+                           batch.obs_q, batch.gs, dict(batch.params, n_max=160), batch.workspace)
+    assert e.value.status in (zipage.ZP_ERR_UNSUPPORTED, zipage.ZP_ERR_INVALID_ARG)
+    with pytest.raises(zipage.ZipageError) as e:   # w*G_q = 33*4 > 128 window rows
+        zipage.zp_compress(batch.pool, batch.d_tables, batch.d_seq, batch.d_qslot, batch.d_dst,
+                           batch.obs_q, batch.gs, dict(batch.params, window=33), batch.workspace)
+    assert e.value.status == zipage.ZP_ERR_UNSUPPORTED
+    before = synth.bf16_bits(batch.pool)
+    zipage.zp_compress(batch.pool, batch.d_tables[:0], batch.d_seq[:0], batch.d_qslot[:0],
+                       batch.d_dst[:0], batch.obs_q, batch.gs, batch.params, batch.workspace)
+    torch.cuda.synchronize()
+    assert np.array_equal(before, synth.bf16_bits(batch.pool))
+    batch.close()
+
+
+def test_wrong_seq_len_is_reported(zp):
+    zipage, runner = zp
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, n_max=8)
+    inp = synth.make_inputs(wl, "cpu")
+    pool_in = synth.bf16_bits(inp.pool)
+    batch = runner.CompressionBatch(inp, "cuda")
+    batch.d_seq[0] = wl.L - 3
+    batch.launch()
+    assert batch.error() == zipage.ZP_ERR_BAD_TABLE
+    out = synth.bf16_bits(batch.pool)
+    for blk in inp.block_tables[0, :wl.n_max]:
+        assert np.array_equal(out[:, blk], pool_in[:, blk])
+    batch.close()
+
+
+# ------------------------------------------------------------------ full-size workloads -----
+
+FULL = ["qwen2_7b", "llama3_8b", "shared_prefix"]
+
+
+def _compaction_property_all_units(batch, pristine, keep):
+    """Every unit: compacted row j equals input row src_j (bit-exact), k kept per head,
+    protected window kept; blocks outside the destination tables are unchanged."""
+    wl = batch.wl
+    b, k, L, w = wl.block_size, (wl.n_max - 1) * wl.block_size, wl.L, wl.window
+    nl, Hkv = wl.num_layers, wl.num_kv_heads
+    counts = keep.sum(-1)
+    assert bool((counts == k).all())
+    if wl.protect_window:
+        assert bool((keep[..., L - w:] == 1).all())
+    dev = batch.pool.device
+    pos = torch.arange(L, device=dev)
+    li = torch.arange(nl, device=dev)[:, None, None]
+    hi = torch.arange(Hkv, device=dev)[None, :, None]
+    for r in range(batch.inp.num_compress):
+        src = pos.expand(nl, Hkv, L)[keep[r].bool()].view(nl, Hkv, k)
+        tab = torch.from_numpy(batch.tables[r]).to(dev).long()
+        dtab = torch.from_numpy(batch.dst_tables[r]).to(dev).long()
+        j = torch.arange(k, device=dev)
+        for kv in (0, 1):
+            old = pristine[li, tab[src // b], kv, hi, src % b]
+            new = batch.pool[li, dtab[j // b][None, None, :], kv, hi, (j % b)[None, None, :]]
+            assert torch.equal(old.view(torch.int16), new.view(torch.int16)), f"request {r} kv {kv}"
+    written = set(batch.dst_tables[:, :wl.n_max - 1].ravel().tolist())
+    others = torch.tensor(sorted(set(range(batch.pool.shape[1])) - written), device=dev)
+    assert torch.equal(pristine[:, others].view(torch.int16), batch.pool[:, others].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_units_and_properties(zp, name):
+    zipage, runner = zp
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl, "cuda")
+    pristine = inp.pool.clone()
+    gs_in = inp.global_scores.clone()
+    batch = runner.CompressionBatch(inp, "cuda", pool=inp.pool)
+    batch.enable_debug()
+    batch.launch()
+    assert batch.error() == 0
+    keep = batch.debug["keep"]
+    _compaction_property_all_units(batch, pristine, keep)
+    # sampled units against the oracle
+    rng = np.random.default_rng(7)
+    R = inp.num_compress
+    units = [(int(rng.integers(R)), int(rng.integers(wl.num_layers)), int(rng.integers(wl.num_kv_heads)))
+             for _ in range(6)] + [(0, 0, 0), (R - 1, wl.num_layers - 1, wl.num_kv_heads - 1)]
+    units = sorted(set(units))
+    reqs = sorted({u[0] for u in units})
+    # oracle inputs restricted to the sampled requests (their blocks only)
+    sub_tables = batch.tables[reqs]
+    sub_dst = batch.dst_tables[reqs]
+    blocks = sorted(set(sub_tables[:, :wl.n_max].ravel().tolist()) | set(sub_dst[:, :wl.n_max].ravel().tolist()))
+    remap = {blk: i for i, blk in enumerate(blocks)}
+    rt = np.vectorize(remap.get)(sub_tables[:, :wl.n_max]).astype(np.int32)
+    rd = np.vectorize(remap.get)(sub_dst[:, :wl.n_max]).astype(np.int32)
+    bidx = torch.tensor(blocks, device="cuda")
+    pool_in = synth.bf16_bits(pristine[:, bidx])
+    pool_out = synth.bf16_bits(batch.pool[:, bidx])
+    qs = torch.tensor(inp.qslot[reqs], device="cuda").long()
+    obs_q = synth.bf16_bits(batch.obs_q[qs])
+    gsi = gs_in[qs].cpu().numpy()
+    gso = batch.gs[qs].cpu().numpy()
+    dbg = {k: v[torch.tensor(reqs, device="cuda")].cpu().numpy() for k, v in batch.debug.items()}
+    ridx = {r: i for i, r in enumerate(reqs)}
+    sub_units = [(ridx[r], l, h) for (r, l, h) in units]
+    p = wl.params()
+    parity.check_units(sub_units, pool_in, obs_q, gsi, rt, rd, inp.seq_len[reqs],
+                       np.arange(len(reqs), dtype=np.int32), p, dbg, gso, pool_out)
+    # shared prefix blocks are byte-identical
+    shared = np.nonzero(inp.refcount > 1)[0]
+    if len(shared):
+        sb = torch.tensor(shared, device="cuda")
+        assert torch.equal(pristine[:, sb].view(torch.int16), batch.pool[:, sb].view(torch.int16))
+    batch.close()

@@ -1,0 +1,139 @@
+"""GPU parity of paged decode attention (zp_paged_decode_attn) and of the mixed serving step:
+compression on a side stream while decode runs on the main stream."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import parity
+from oracle import zipage_oracle as O
+from paged_kv_cache_obs_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+# bf16 output: rounding is at most 2^-9 relative; fp32 accumulation adds far less
+DEC_RTOL, DEC_ATOL = 4e-3, 1e-4
+
+
+@pytest.fixture(scope="module")
+def zp():
+    import os
+    from paged_kv_cache_obs_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from paged_kv_cache_obs_gb300 import runner, zipage
+    return zipage, runner
+
+
+def _decode_case(zipage, Hq, Hkv, d, b, seq_lens, layers=2, seed=0, layer=1):
+    g = torch.Generator().manual_seed(seed)
+    B = len(seq_lens)
+    max_blocks = max((s + b - 1) // b for s in seq_lens) + 1
+    NB = B * max_blocks + 7
+    pool = torch.randn((layers, NB, 2, Hkv, b, d), generator=g).to(torch.bfloat16)
+    perm = torch.randperm(NB, generator=g).numpy().astype(np.int32)
+    tables = perm[:B * max_blocks].reshape(B, max_blocks).copy()
+    q = torch.randn((B, Hq, d), generator=g).to(torch.bfloat16)
+    p = dict(num_layers=layers, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=b, n_max=max_blocks,
+             window=1, alpha=0.5, beta=0.5, decay=0.9, scale=1.0 / np.sqrt(d), protect_window=1, causal=1)
+    dp, dq = pool.cuda(), q.cuda()
+    dt = torch.from_numpy(tables).cuda()
+    ds = torch.tensor(seq_lens, dtype=torch.int32).cuda()
+    out = torch.zeros((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+    ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, B, max_blocks))
+    zipage.zp_paged_decode_attn(dp, layer, dq, dt, ds, out, p, ws)
+    assert zipage.zp_read_error(ws) == 0
+    got = O.bf16_bits_to_f64(synth.bf16_bits(out))
+    pb, qb = synth.bf16_bits(pool), synth.bf16_bits(q)
+    G = Hq // Hkv
+    for r, s in enumerate(seq_lens):
+        for h in range(Hkv):
+            k = O.gather_rows(pb, layer, 0, h, tables[r], s, b)
+            v = O.gather_rows(pb, layer, 1, h, tables[r], s, b)
+            want = O.decode_attention(qb[r, h * G:(h + 1) * G], k, v, p["scale"])
+            err = np.abs(got[r, h * G:(h + 1) * G] - want)
+            assert (err <= DEC_RTOL * np.abs(want) + DEC_ATOL).all(), (r, h, float(err.max()))
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,b", [(32, 8, 128, 16), (28, 4, 128, 32), (8, 8, 64, 16), (16, 2, 64, 32),
+                                        (8, 4, 128, 16)])
+def test_decode_matches_oracle(zp, Hq, Hkv, d, b):
+    zipage, _ = zp
+    _decode_case(zipage, Hq, Hkv, d, b, [1, b - 1, b, b + 1, 255, 256, 257, 700])
+
+
+def test_decode_long_sequences_many_splits(zp):
+    zipage, _ = zp
+    _decode_case(zipage, 32, 8, 128, 16, [2048, 2047, 1500, 33], seed=3)
+
+
+def test_decode_bad_block_id_reports(zp):
+    zipage, _ = zp
+    p = dict(num_layers=1, num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16, n_max=4, window=1,
+             alpha=0.5, beta=0.5, decay=0.9, scale=0.125, protect_window=1, causal=1)
+    pool = torch.zeros((1, 8, 2, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    tables = torch.tensor([[0, 1, 99, 2]], dtype=torch.int32, device="cuda")
+    seq = torch.tensor([50], dtype=torch.int32, device="cuda")
+    q = torch.zeros((1, 4, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros_like(q)
+    ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, 1, 4))
+    zipage.zp_paged_decode_attn(pool, 0, q, tables, seq, out, p, ws)
+    assert zipage.zp_read_error(ws) == zipage.ZP_ERR_BAD_TABLE
+
+
+def test_mixed_step_side_stream(zp):
+    """Compression of the slot holders on a side stream, decode of the others on the main
+    stream, then the event-deferred release of the last blocks."""
+    zipage, runner = zp
+    wl = synth.WORKLOADS["mixed"].scaled(num_requests=4, num_layers=3, num_decode=12)
+    inp = synth.make_inputs(wl, "cpu")
+    pool_in = synth.bf16_bits(inp.pool)
+    obs_q = synth.bf16_bits(inp.obs_q)
+    gs_in = inp.global_scores.numpy()
+    R = inp.num_compress
+    batch = runner.CompressionBatch(inp, "cuda")
+    batch.enable_debug()
+    p = wl.params()
+    dec_tables = torch.from_numpy(np.ascontiguousarray(inp.block_tables[R:])).cuda()
+    dec_seq = torch.from_numpy(np.ascontiguousarray(inp.seq_len[R:])).cuda()
+    nd = wl.num_decode
+    dq = inp.decode_q.cuda()
+    outs = torch.zeros((wl.num_layers, nd, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    ws = [zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, nd, wl.n_max)) for _ in range(wl.num_layers)]
+    side = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    free_before = zipage.zp_num_free(batch.alloc)
+    with torch.cuda.stream(side):
+        batch.launch(stream=side)
+        batch.commit(stream=side)       # last blocks released only when the side stream is done
+    for l in range(wl.num_layers):
+        zipage.zp_paged_decode_attn(batch.pool, l, dq[l], dec_tables, dec_seq, outs[l], p, ws[l], stream=main)
+    assert zipage.zp_num_pending(batch.alloc) >= 0
+    side.synchronize()
+    main.synchronize()
+    zipage.zp_alloc_drain(batch.alloc)
+    assert zipage.zp_num_pending(batch.alloc) == 0
+    assert zipage.zp_num_free(batch.alloc) == free_before + R
+    assert batch.error(stream=side) == 0
+    for w_ in ws:
+        assert zipage.zp_read_error(w_) == 0
+    # decode results: the decode requests' blocks are disjoint from the compressing ones
+    got = O.bf16_bits_to_f64(synth.bf16_bits(outs))
+    qb = synth.bf16_bits(inp.decode_q)
+    G = wl.num_q_heads // wl.num_kv_heads
+    for l in range(wl.num_layers):
+        for i in range(nd):
+            r = R + i
+            s = int(inp.seq_len[r])
+            for h in range(wl.num_kv_heads):
+                k = O.gather_rows(pool_in, l, 0, h, inp.block_tables[r], s, wl.block_size)
+                v = O.gather_rows(pool_in, l, 1, h, inp.block_tables[r], s, wl.block_size)
+                want = O.decode_attention(qb[l, i, h * G:(h + 1) * G], k, v, wl.scale)
+                err = np.abs(got[l, i, h * G:(h + 1) * G] - want)
+                assert (err <= DEC_RTOL * np.abs(want) + DEC_ATOL).all()
+    # compression results, every unit and every pool byte
+    units = [(r, l, h) for r in range(R) for l in range(wl.num_layers) for h in range(wl.num_kv_heads)]
+    dbg = {k: v.cpu().numpy() for k, v in batch.debug.items()}
+    parity.check_units(units, pool_in, obs_q, gs_in, batch.tables, batch.dst_tables, inp.seq_len[:R],
+                       inp.qslot, p, dbg, batch.gs.cpu().numpy(), synth.bf16_bits(batch.pool), full_pool=True)
+    batch.close()
