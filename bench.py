@@ -205,7 +205,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
-    wl = synth.WORKLOADS[args.workload]
+    wl = workload_of(args)
     inp = synth.make_inputs(wl, "cuda", seed=synth.seed_of(wl) + 1000 * rank)
     pristine_pool = inp.pool.clone()
     pristine_gs = inp.global_scores.clone()
@@ -386,13 +386,23 @@ def run_cpu_baseline(inp, pool, gs):
 
 # ------------------------------------------------------------------ reference arm -----------
 
+def workload_of(args):
+    from paged_kv_cache_obs_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.requests:
+        wl = wl.scaled(num_requests=args.requests)
+    if args.layers:
+        wl = wl.scaled(num_layers=args.layers)
+    return wl
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import torch
     from paged_kv_cache_obs_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
+    wl = workload_of(args)
     # the same inputs as our arm, drawn on the CPU for the sampled requests only
     small = wl.scaled(num_requests=2)
     inp = synth.make_inputs(small, "cpu", seed=synth.seed_of(wl))
@@ -424,6 +434,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=0, help="override the workload's request count (profiling)")
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
