@@ -60,6 +60,10 @@ struct CompressArgs {
   int32_t* dbg_keep;
   int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, E, max_blocks, num_qslots;
   float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
+  float inv_rw, inv_bm1;          // 1 / (w * G_q), 1 / (b - 1)
+  uint32_t block_bytes;           // bytes of one (layer, block): 2 * Hkv * b * d * 2
+  uint32_t kv_bytes;              // bytes of the K (or V) part of a block: Hkv * b * d * 2
+  uint32_t row_bytes;             // d * 2
   int protect_window, causal;
 };
 
@@ -77,18 +81,17 @@ struct __align__(1024) Smem {
       unsigned long long wcand[kKeysPerCta];    // per-warp candidates
     } sel;
   } u1;
-  unsigned long long cand_recv[kMaxCluster][kMaxEvict];
+  unsigned long long cand_recv[kMaxCluster * kMaxEvict];  // [cta * E + rank]
   int status_recv[kMaxCluster];
   float row_off[kRows];
   int evict_pos[kMaxEvict];
   int src_tab[kMaxTable];
   int dst_tab[kMaxTable];
-  int move_list[kKeysPerCta];       // (local key << 16) | destination slot
-  int warp_count[kThreads / 32];
+  int dst_of[kKeysPerCta];          // destination slot of each key that moves, else -1
   uint64_t bar_tma;
   uint64_t bar_mma;
+  uint64_t bar_v;
   uint32_t tmem_base;
-  int n_move;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -119,10 +122,10 @@ __device__ __forceinline__ void record_error(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-__device__ __forceinline__ size_t row_offset_bytes(const CompressArgs& a, int layer, int phys, int kv, int h,
-                                                   int row) {
-  const int64_t tile = ((static_cast<int64_t>(layer) * a.num_blocks + phys) * 2 + kv) * a.Hkv + h;
-  return static_cast<size_t>((tile * a.b + row) * a.d) * 2;
+// Byte offset of row `row` of block `phys`, relative to this unit's head base (layer, K, head).
+__device__ __forceinline__ size_t row_off_bytes(const CompressArgs& a, int phys, int kv, int row) {
+  return static_cast<size_t>(static_cast<uint32_t>(phys)) * a.block_bytes + kv * a.kv_bytes +
+         static_cast<uint32_t>(row) * a.row_bytes;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -142,15 +145,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int t0 = c * kKeysPerCta;
   const int nk = min(kKeysPerCta, L - t0);
   const int nhalf = d / 64;
+  uint8_t* const head_base = a.pool + static_cast<size_t>(layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
+                             static_cast<size_t>(h) * b * a.row_bytes;
 
   // ---------------------------------------------------------------- set-up --------------
   if (tid == 0) {
     mbar_init(&s.bar_tma, 1);
     mbar_init(&s.bar_mma, 1);
+    mbar_init(&s.bar_v, 1);
     fence_mbar_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmQ);
   }
+  __syncwarp();
   if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
 
   // Validate the request's metadata; every CTA of the cluster sees the same values, so they
@@ -177,17 +184,20 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (skip && tid == 0 && c == 0) record_error(a.err, ZP_ERR_BAD_TABLE);
   const uint32_t tbase = s.tmem_base;
 
-  const int kt = t0 + tid;  // the key this thread owns in passes 2..6
+  const int kt = t0 + tid;  // the key this thread owns from pass 2 on
   const bool key_valid = tid < nk;
   float g_in = 0.0f;
-  int jdst = -1;  // destination slot of this thread's key if kept
-  bool fail = false;
+  float attn = 0.0f, red = 0.0f, S = 0.0f;
+  bool ok = true;  // outcome of the bounded waits, meaningful in the waiting thread (tid 0)
 
+  // ---- step 1: TMA of K and Q, then D1 = Q K^T (M = 128 window rows, N = nk keys).  Only
+  //      thread 0 waits on the mbarriers; the others block on the CTA barrier below.
   if (!skip) {
-    if (key_valid)
-      g_in = a.gscores[((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L + kt];
+    if (key_valid) g_in = a.gscores[((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L + kt];
     if (tid == 0) {
       mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nk + Rw) * d * 2));
+      for (int hd = 0; hd < nhalf; ++hd)
+        tma_load_3d(&s.Q[hd][0], &tmQ, &s.bar_tma, hd * 64, h * Gq, (slot * a.layers + layer) * w);
       const int nblk = nk / b;
       for (int bi = 0; bi < nblk; ++bi) {
         const int phys = s.src_tab[t0 / b + bi];
@@ -195,13 +205,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           tma_load_3d(&s.K[hd][bi * b * 128], &tmK, &s.bar_tma, hd * 64, h * b,
                       layer * static_cast<int>(a.num_blocks) + phys);
       }
-      for (int hd = 0; hd < nhalf; ++hd)
-        tma_load_3d(&s.Q[hd][0], &tmQ, &s.bar_tma, hd * 64, h * Gq, (slot * a.layers + layer) * w);
-    }
-    fail |= !mbar_wait_bounded(&s.bar_tma, 0, kWaitNs);
-
-    // ---- D1 = Q K^T: M = 128 window rows, N = nk keys -> TMEM columns [0, nk)
-    if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_tma, 0, kWaitNs);
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(128, nk);
       for (int kk = 0; kk < d / 16; ++kk) {
@@ -210,51 +214,82 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_bf16(tbase, ad, bd, idesc, kk > 0);
       }
       mma_commit(&s.bar_mma);
-    }
-    fail |= !mbar_wait_bounded(&s.bar_mma, 0, kWaitNs);
-    tc_fence_after();
-
-    // ---- pass 1: per-row max and exp-sum over this CTA's keys (thread = row, half of columns)
-    {
-      const int i = q4 * 32 + lane;
-      const bool row_ok = i < Rw;
-      const int t_lim = a.causal ? (L - w + i / Gq) : (L - 1);
-      float m = -INFINITY;
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int col0 = hh * 128 + c4 * 32;
-        if (col0 >= nk) break;
-        float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + col0, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const bool ok = row_ok && (col0 + j < nk) && (t0 + col0 + j <= t_lim);
-          if (ok) m = fmaxf(m, v[j]);
-        }
-      }
-      // second sweep: every lane runs the same collective loads; rows without a visible key
-      // never pass the predicate, so their -inf maximum is never used
-      float l = 0.0f;
-      const float mo = m * a.sl2;
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int col0 = hh * 128 + c4 * 32;
-        if (col0 >= nk) break;
-        float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + col0, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const bool ok = row_ok && (col0 + j < nk) && (t0 + col0 + j <= t_lim);
-          if (ok) l += ex2(fmaf(v[j], a.sl2, -mo));
-        }
-      }
-      s.u0.part[hh][i] = make_float2(m, l);
+      ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
     }
   }
-  tc_fence_before();
-  fail = __syncthreads_or(fail);
+  bool fail = __syncthreads_or(!ok);
   tc_fence_after();
 
+  // ---- step 2 (pass 1): per-row max and exp-sum over this CTA's keys.  Thread = window row
+  //      (TMEM lane), warp half hh = 128 key columns; two 32-column loads per wait; chunks that
+  //      every row sees completely take the unpredicated path.
   if (!skip) {
-    // Gram of each 128-key half: TMEM columns [128*kh, 128*kh + 128); D1 is fully read.
+    const int i = q4 * 32 + lane;
+    const int t_lim = a.causal ? (L - w + i / Gq) : (L - 1);
+    const int vis_all = a.causal ? (L - w) : (L - 1);  // keys every window row sees
+    const int cbase = hh * 128;
+    const int ncol = nk - cbase;                         // valid columns of this half (may be <= 0)
+    const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int col0 = c2 * 64;
+      if (col0 >= ncol) break;
+      uint32_t ra[32], rb[32];
+      tmem_ld32_issue(tl + col0, ra);
+      tmem_ld32_issue(tl + col0 + 32, rb);
+      tmem_wait_ld(ra);
+      tmem_ld_dep(rb);
+      if (col0 + 64 <= ncol && t0 + cbase + col0 + 63 <= vis_all) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+          mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int cc = col0 + j;
+          const float v = __uint_as_float(j < 32 ? ra[j & 31] : rb[j & 31]);
+          if (cc < ncol && t0 + cbase + cc <= t_lim) mx[j & 3] = fmaxf(mx[j & 3], v);
+        }
+      }
+    }
+    const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    const float mo = m * a.sl2;
+    float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int col0 = c2 * 64;
+      if (col0 >= ncol) break;
+      uint32_t ra[32], rb[32];
+      tmem_ld32_issue(tl + col0, ra);
+      tmem_ld32_issue(tl + col0 + 32, rb);
+      tmem_wait_ld(ra);
+      tmem_ld_dep(rb);
+      if (col0 + 64 <= ncol && t0 + cbase + col0 + 63 <= vis_all) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
+          ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int cc = col0 + j;
+          const float v = __uint_as_float(j < 32 ? ra[j & 31] : rb[j & 31]);
+          if (cc < ncol && t0 + cbase + cc <= t_lim) ls[j & 3] += ex2(fmaf(v, a.sl2, -mo));
+        }
+      }
+    }
+    // rows without a visible key keep m = -inf and l = 0; padding rows are dropped below
+    s.u0.part[hh][i] = make_float2(m, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- step 3: Gram of each 128-key half into TMEM (D1 fully read) while the row partials
+  //      go to every CTA of the cluster.
+  if (!skip) {
     if (tid == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
       for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
@@ -264,10 +299,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       mma_commit(&s.bar_mma);
     }
-    // merge the two column halves and push (max, sum) of each row to every CTA
     if (tid < kRows) {
       const float2 p0 = s.u0.part[0][tid], p1 = s.u0.part[1][tid];
       float m = fmaxf(p0.x, p1.x), l = 0.0f;
+      if (tid >= Rw) m = -INFINITY;  // padding row of the MMA, not a window row
       if (m != -INFINITY) {
         if (p0.y > 0.0f) l += p0.y * ex2((p0.x - m) * a.sl2);
         if (p1.y > 0.0f) l += p1.y * ex2((p1.x - m) * a.sl2);
@@ -278,7 +313,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   cluster_sync();  // #1: every CTA's row partials have landed
 
-  float attn = 0.0f, red = 0.0f, S = 0.0f;
   if (!skip) {
     if (tid < kRows) {
       float M = -INFINITY;
@@ -291,23 +325,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       s.row_off[tid] = (tid < Rw && Lsum > 0.0f) ? fmaf(M, a.sl2, lg2(Lsum)) : INFINITY;
     }
+    if (tid == 0) ok = mbar_wait_bounded(&s.bar_mma, 1, kWaitNs) && ok;
+  }
+  fail |= __syncthreads_or(!ok);
+  tc_fence_after();
 
-    // ---- Lightning redundancy from the Gram (thread = key)
-    fail |= !mbar_wait_bounded(&s.bar_mma, 1, kWaitNs);
-    tc_fence_after();
-    float gv[32];
+  // ---- step 4: Lightning redundancy from the Gram (thread = key)
+  float gv[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) gv[j] = 0.0f;
-    const int wcol = hh * 128 + q4 * 32;  // first key (and Gram column) of this warp
+  for (int j = 0; j < 32; ++j) gv[j] = 0.0f;
+  const int wcol = hh * 128 + q4 * 32;  // first key (and Gram column) of this warp
+  float inv_nt = 0.0f;
+  if (!skip) {
     if (wcol < nk) tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + wcol, gv);
     float diag = 0.0f;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (j == lane) diag = gv[j];
-    s.u0.norm[tid] = fmaxf(sqrtf(fmaxf(diag, 0.0f)), 1e-12f);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    inv_nt = 1.0f / fmaxf(sqrtf(fmaxf(diag, 0.0f)), 1e-12f);
+    s.u0.norm[tid] = inv_nt;  // reciprocal key norms
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (!skip) {
     // D2 = K Q^T per 128-key half into the same TMEM columns (Gram fully read)
     if (tid == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
@@ -320,54 +361,106 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_commit(&s.bar_mma);
     }
     if (key_valid) {
-      const int jb0 = (tid % 32) / b * b;  // first column of this key's block within gv
-      const float nt = s.u0.norm[tid];
-      float acc = 0.0f;
+      const int jb0 = (tid & 31) / b * b;  // first column of this key's block within gv
+      const float4* inv4 = reinterpret_cast<const float4*>(&s.u0.norm[tid & ~31]);
+      float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j >= jb0 && j < jb0 + b && j != lane) acc += gv[j] / (nt * s.u0.norm[(tid & ~31) + j]);
-      red = acc / static_cast<float>(b - 1);
-    }
-
-    // ---- pass 2: attention mass of this key over the window rows
-    fail |= !mbar_wait_bounded(&s.bar_mma, 0, kWaitNs);
-    tc_fence_after();
-    if (wcol < nk) {
-      const int imin = a.causal ? max(0, Gq * (kt - (L - w))) : 0;
-      float acc = 0.0f;
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128 + c4 * 32, v);
+      for (int q = 0; q < 8; ++q) {
+        const float4 nv = inv4[q];
+        const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int i = c4 * 32 + j;
-          if (i >= imin) acc += ex2(fmaf(v[j], a.sl2, -s.row_off[i]));
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * q + e;
+          const float cv = (j >= jb0 && j < jb0 + b && j != lane) ? gv[j] * nn[e] : 0.0f;
+          if (e & 1) acc1 += cv; else acc0 += cv;
         }
       }
-      attn = acc / static_cast<float>(Rw);
+      red = (acc0 + acc1) * inv_nt * a.inv_bm1;
+    }
+    if (tid == 0) ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
+  }
+  fail |= __syncthreads_or(!ok);
+  tc_fence_after();
+
+  // ---- step 5: Q is no longer needed: stage V rows [0, min(128, nk)) into its place by bulk
+  //      copies (one per block), then pass 2, then V rows [128, nk) into registers.  All of it
+  //      completes before the second cluster barrier, which therefore also separates every
+  //      read of the unit from every write.
+  uint8_t* const vstage = &s.Q[0][0];
+  const int nv0 = min(128, nk);
+  if (!skip && tid == 0) {
+    mbar_arrive_expect_tx(&s.bar_v, static_cast<uint32_t>(nv0) * a.row_bytes);
+    for (int bi = 0; bi < nv0 / b; ++bi) {
+      const uint8_t* src = head_base + row_off_bytes(a, s.src_tab[t0 / b + bi], 1, 0);
+      bulk_load(vstage + static_cast<size_t>(bi) * b * a.row_bytes, src, static_cast<uint32_t>(b) * a.row_bytes,
+                &s.bar_v);
+    }
+  }
+  __syncwarp();  // warp 0 reconverges before the collective TMEM loads
+  if (!skip) {
+    // pass 2: attention mass of this key over the window rows.  Thread = key (TMEM lane),
+    // columns = window rows; rows beyond R_w have row_off = +inf and add 0.
+    if (wcol < nk) {
+      const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128;
+      const bool all_rows = !a.causal || (t0 + wcol + 31 <= L - w);
+      const int imin = a.causal ? max(0, Gq * (kt - (L - w))) : 0;
+      const float4* off4 = reinterpret_cast<const float4*>(s.row_off);
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int c2 = 0; c2 < 2; ++c2) {
+        if (c2 * 64 >= Rw) break;
+        uint32_t ra[32], rb[32];
+        tmem_ld32_issue(tl + c2 * 64, ra);
+        tmem_ld32_issue(tl + c2 * 64 + 32, rb);
+        tmem_wait_ld(ra);
+        tmem_ld_dep(rb);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 o = off4[c2 * 16 + q];
+          const float oo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int jj = 4 * q + e;  // 0..63 within this pair of loads
+            const float v = __uint_as_float(jj < 32 ? ra[jj & 31] : rb[jj & 31]);
+            const float p = ex2(fmaf(v, a.sl2, -oo[e]));
+            if (all_rows || c2 * 64 + jj >= imin) acc[e] += p;
+          }
+        }
+      }
+      attn = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * a.inv_rw;
     }
     S = (attn + a.alpha * g_in) - a.beta * red;
     if (a.protect_window && kt >= L - w) S = INFINITY;
-
     if (key_valid) {
       const int64_t o = ((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt;
       if (a.dbg_attn) a.dbg_attn[o] = attn;
       if (a.dbg_redund) a.dbg_redund[o] = red;
       if (a.dbg_score) a.dbg_score[o] = S;
     }
+  }
+  // V rows [128, nk): warp w holds rows 128 + 16w .. 128 + 16w + 15 (rpi rows per load)
+  const int cpr = d / 8, rpi = 32 / cpr;
+  uint4 vreg[8];
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    vreg[it] = make_uint4(0, 0, 0, 0);
+    const int row = 128 + warp * 16 + it * rpi + lane / cpr, ch = lane % cpr;
+    if (!skip && it * rpi < 16 && row < nk) {
+      const int t = t0 + row;
+      vreg[it] = *reinterpret_cast<const uint4*>(head_base + row_off_bytes(a, s.src_tab[t / b], 1, t % b) + ch * 16);
+    }
+  }
 
-    // ---- selection, level 1: per-warp bottom-E by rank counting over the warp's 32 keys
+  // ---- step 6: selection, level 1: per-warp bottom-E by rank counting over the warp's keys
+  if (!skip) {
     const int E = a.E;
     const unsigned long long mykey = key_valid ? evict_key(S, kt) : (~0ull - static_cast<unsigned long long>(tid));
     int wr = 0;
-#pragma unroll 8
+#pragma unroll
     for (int u = 0; u < 32; ++u) wr += (__shfl_sync(0xffffffffu, mykey, u) < mykey) ? 1 : 0;
     const int wE = min(E, 32);
     if (wr < wE) s.u1.sel.wcand[warp * wE + wr] = mykey;
   }
-  tc_fence_before();
-  fail = __syncthreads_or(fail);
-  tc_fence_after();
+  __syncthreads();
 
   if (!skip) {
     // level 2: rank each warp candidate among all of this CTA's warp candidates
@@ -375,19 +468,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int ncand = (kThreads / 32) * min(E, 32);
     if (tid < ncand) {
       const unsigned long long key = s.u1.sel.wcand[tid];
+      const ulonglong2* w2 = reinterpret_cast<const ulonglong2*>(s.u1.sel.wcand);
       int rk = 0;
-      for (int u = 0; u < ncand; ++u) rk += (s.u1.sel.wcand[u] < key) ? 1 : 0;
+#pragma unroll 4
+      for (int u = 0; u < ncand / 2; ++u) {
+        const ulonglong2 kk = w2[u];
+        rk += (kk.x < key) + (kk.y < key);
+      }
       if (rk < E) {
-        const uint32_t local = smem_u32(&s.cand_recv[c][rk]);
+        const uint32_t local = smem_u32(&s.cand_recv[c * E + rk]);
         for (int dst = 0; dst < C; ++dst) st_cluster_u64(mapa(local, dst), key);
       }
     }
     if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_v, 0, kWaitNs) && ok;  // staged V rows have landed
       const uint32_t local = smem_u32(&s.status_recv[c]);
-      for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), fail ? 1u : 0u);
+      for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), (fail || !ok) ? 1u : 0u);
     }
   }
-  cluster_sync();  // #2: candidates and statuses of every CTA have landed
+  cluster_sync();  // #2: candidates, statuses and every read of every CTA of the unit are done
 
   bool any_fail = false;
   if (!skip) {
@@ -396,16 +495,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int ntot = C * E;
     // level 3: the E lowest keys of the cluster, identical in every CTA
     if (tid < ntot) {
-      const unsigned long long key = s.cand_recv[tid / E][tid % E];
+      const unsigned long long key = s.cand_recv[tid];
+      const ulonglong2* c2v = reinterpret_cast<const ulonglong2*>(s.cand_recv);
       int rk = 0;
-      for (int u = 0; u < ntot; ++u) rk += (s.cand_recv[u / E][u % E] < key) ? 1 : 0;
+#pragma unroll 4
+      for (int u = 0; u < ntot / 2; ++u) {
+        const ulonglong2 kk = c2v[u];
+        rk += (kk.x < key) + (kk.y < key);
+      }
       if (rk < E) s.evict_pos[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
     }
     __syncthreads();
 
-    // destination of this CTA's keys: j = t - #(evicted before t)
-    bool evicted = false, moved = false;
-    int j = 0;
+    // destination of this CTA's keys: j = t - #(evicted before t); -1 = nothing to move
+    int j = -1;
+    bool evicted = false;
     if (key_valid) {
       int shift = 0;
       for (int e = 0; e < E; ++e) {
@@ -413,74 +517,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         shift += (p < kt) ? 1 : 0;
         evicted |= (p == kt);
       }
-      j = kt - shift;
       if (!evicted) {
-        const int sp = s.src_tab[kt / b], dp = s.dst_tab[j / b];
-        moved = (sp != dp) || (kt % b != j % b);
+        j = kt - shift;
+        g_in = a.decay * g_in + attn;  // global-score update of the kept key
       }
       if (a.dbg_keep)
         a.dbg_keep[((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt] = evicted ? 0 : 1;
     }
-    // compact list of moved keys (warp ballot + scan over the 8 warps)
-    const unsigned ball = __ballot_sync(0xffffffffu, moved);
-    if (lane == 0) s.warp_count[warp] = __popc(ball);
-    __syncthreads();
-    int base = 0, total = 0;
-    for (int ww = 0; ww < kThreads / 32; ++ww) {
-      base += (ww < warp) ? s.warp_count[ww] : 0;
-      total += s.warp_count[ww];
-    }
-    if (moved) s.move_list[base + __popc(ball & ((1u << lane) - 1))] = (tid << 16) | j;
-    if (tid == 0) s.n_move = total;
+    const bool moved = j >= 0 && (s.src_tab[kt / b] != s.dst_tab[j / b] || kt % b != j % b);
+    s.dst_of[tid] = moved ? j : -1;
     __syncthreads();
 
-    // global-score update of kept keys; written after the barrier
-    if (key_valid && !evicted) {
-      g_in = a.decay * g_in + attn;
-      jdst = j;
-    }
-  }
-
-  // ---- V rows that move: into registers before the barrier (warp w owns list entries
-  //      [32w, 32w+32); cpr 16-byte chunks per row, rpi rows per warp iteration)
-  const int cpr = d / 8, rpi = 32 / cpr, iters = 32 / rpi;
-  uint4 vbuf[16];
-  if (!skip) {
-    const int n_move = s.n_move;
+    if (!any_fail) {
+      // K from shared memory (swizzled rows), V from the staging area or registers.  Warp w
+      // writes rows 16w .. 16w + 15 and 128 + 16w .. 128 + 16w + 15.
+      const int ch = lane % cpr, half = ch >> 3, c8 = ch & 7;
 #pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int e = warp * 32 + it * rpi + lane / cpr, ch = lane % cpr;
-      vbuf[it] = make_uint4(0, 0, 0, 0);
-      if (it < iters && e < n_move) {
-        const int kl = s.move_list[e] >> 16;
-        const int t = t0 + kl;
-        const uint8_t* src = a.pool + row_offset_bytes(a, layer, s.src_tab[t / b], 1, h, t % b) + ch * 16;
-        vbuf[it] = *reinterpret_cast<const uint4*>(src);
-      }
-    }
-  }
-  cluster_sync();  // #3: every read of the unit (K by TMA, V, G) precedes every write
-
-  if (!skip && !any_fail) {
-    const int n_move = s.n_move;
+      for (int it = 0; it < 8; ++it) {
+        if (it * rpi >= 16) break;
+        const int sub = it * rpi + lane / cpr;
 #pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int e = warp * 32 + it * rpi + lane / cpr, ch = lane % cpr;
-      if (it < iters && e < n_move) {
-        const int packed = s.move_list[e];
-        const int kl = packed >> 16, jj = packed & 0xFFFF;
-        const int dp = s.dst_tab[jj / b];
-        const int half = ch >> 3, c8 = ch & 7;
-        const uint4 kv = *reinterpret_cast<const uint4*>(&s.K[half][kl * 128 + ((c8 ^ (kl & 7)) << 4)]);
-        uint8_t* dk = a.pool + row_offset_bytes(a, layer, dp, 0, h, jj % b) + ch * 16;
-        uint8_t* dv = a.pool + row_offset_bytes(a, layer, dp, 1, h, jj % b) + ch * 16;
-        *reinterpret_cast<uint4*>(dk) = kv;
-        *reinterpret_cast<uint4*>(dv) = vbuf[it];
+        for (int part = 0; part < 2; ++part) {
+          const int row = part * 128 + warp * 16 + sub;
+          if (row >= nk) continue;
+          const int jj = s.dst_of[row];
+          if (jj < 0) continue;
+          const uint4 kv = *reinterpret_cast<const uint4*>(&s.K[half][row * 128 + ((c8 ^ (row & 7)) << 4)]);
+          const uint4 vv = part == 0 ? *reinterpret_cast<const uint4*>(vstage + row * a.row_bytes + ch * 16) : vreg[it];
+          uint8_t* dk = head_base + row_off_bytes(a, s.dst_tab[jj / b], 0, jj % b) + ch * 16;
+          *reinterpret_cast<uint4*>(dk) = kv;
+          *reinterpret_cast<uint4*>(dk + a.kv_bytes) = vv;
+        }
       }
+      float* G = a.gscores + ((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L;
+      if (j >= 0) G[j] = g_in;
+      if (c == C - 1 && tid < a.E) G[a.k + tid] = 0.0f;
     }
-    float* G = a.gscores + ((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L;
-    if (jdst >= 0) G[jdst] = g_in;
-    if (c == C - 1 && tid < a.E) G[a.k + tid] = 0.0f;
   }
   if (!skip && any_fail && tid == 0 && c == 0) record_error(a.err, ZP_ERR_TIMEOUT);
 
@@ -577,6 +649,11 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.beta = p->beta;
   a.decay = p->decay;
   a.sl2 = p->scale * 1.4426950408889634f;
+  a.inv_rw = 1.0f / static_cast<float>(Rw);
+  a.inv_bm1 = 1.0f / static_cast<float>(b - 1);
+  a.row_bytes = static_cast<uint32_t>(d) * 2;
+  a.kv_bytes = static_cast<uint32_t>(Hkv) * b * a.row_bytes;
+  a.block_bytes = 2 * a.kv_bytes;
   a.protect_window = p->protect_window;
   a.causal = p->causal;
 
