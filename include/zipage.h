@@ -44,7 +44,8 @@ enum {
   ZP_ERR_BAD_TABLE = 3,    /* (device) a block id, seq_len or query slot is out of range */
   ZP_ERR_TIMEOUT = 4,      /* (device) a bounded wait inside a kernel gave up */
   ZP_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
-  ZP_ERR_UNSUPPORTED = 6   /* valid arguments outside what this build implements */
+  ZP_ERR_UNSUPPORTED = 6,  /* valid arguments outside what this build implements */
+  ZP_ERR_TOO_LARGE = 7     /* the call needs more scratch than zp_paged_decode_attn_static holds */
 };
 
 /* Opaque stream handle: a cudaStream_t (CUstream) passed through as a pointer, NULL = legacy
@@ -145,6 +146,35 @@ zp_status zp_paged_decode_attn(const zp_kv_pool* pool, int32_t layer, const uint
                                void* workspace, size_t workspace_bytes, zp_stream stream);
 
 size_t zp_paged_decode_workspace_size(const zp_params* params, int32_t B, int32_t max_blocks);
+
+/* ---------------------------------------------------------------------------------------
+ * zp_paged_decode_attn without any device allocation by anyone.  The paper has no
+ * counterpart: this is a convenience of this library.
+ *
+ * For callers that cannot allocate device memory: a host runtime that owns every device
+ * buffer through its own pool and hands this library no allocator, a serving loop that must
+ * not call cudaMalloc (which can synchronise the whole device) in its hot path, or a process
+ * that must know its complete device footprint when the library is loaded.
+ *
+ * Same operation and arguments as zp_paged_decode_attn, except that the split-KV partials
+ * live in a fixed 16 MiB array inside the library (held by every GPU that loads it until the
+ * process exits), so no workspace is passed.  A call needs
+ * B * H_q * ceil(max_blocks / 16) * (head_dim + 2) * 4 bytes of it, at most 16 MiB - 256 B;
+ * larger calls return ZP_ERR_TOO_LARGE and launch nothing.
+ *   dev_status  device int32 written with the call's device-side status (0, or
+ *               ZP_ERR_BAD_TABLE for a block id outside the pool or a bad seq_len); it is
+ *               cleared on the stream before the kernel runs.  May be NULL, in which case
+ *               device-side errors are not reported.
+ * The first call on a device looks up the array's device address for that device (with the
+ * device current); make that first call before any stream capture.  Every call shares the
+ * one array: calls whose kernels may overlap on the GPU (different streams without an
+ * ordering between them) race on it and must be serialised by the caller.  The call
+ * allocates and frees nothing.
+ * --------------------------------------------------------------------------------------- */
+zp_status zp_paged_decode_attn_static(const zp_kv_pool* pool, int32_t layer, const uint16_t* q,
+                                      const int32_t* block_tables, const int32_t* seq_lens, int32_t B,
+                                      int32_t max_blocks, uint16_t* out, const zp_params* params,
+                                      int32_t* dev_status, zp_stream stream);
 
 /* Synchronises `stream`, copies the error word at the start of `workspace` to *out_status and
  * clears it.  Returns ZP_ERR_CUDA if the copy fails. */

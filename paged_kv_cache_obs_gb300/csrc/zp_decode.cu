@@ -17,6 +17,8 @@
 #include "zp_internal.h"
 #include "zp_ptx.cuh"
 
+#include <mutex>
+
 namespace zp {
 namespace {
 
@@ -352,4 +354,49 @@ extern "C" zp_status zp_paged_decode_attn(const zp_kv_pool* pool, int32_t layer,
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
   return decode_launch(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p, part,
                        static_cast<int32_t*>(workspace), st);
+}
+
+// ------------------------------------------------------------------ no-allocation variant ----
+//
+// Scratch for zp_paged_decode_attn_static: the split-KV partials (and a spare error word) of
+// decode attention live in this fixed device array instead of a caller workspace.  Every GPU
+// that loads the library holds these 16 MiB until the process exits.  In host code the name
+// is only a host-side stand-in; the device address is obtained with cudaGetSymbolAddress,
+// once per device, while that device is current.
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+constexpr size_t kStaticErrBytes = 256;  // spare error word when the caller passes no status
+constexpr int kMaxDevicesStatic = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevicesStatic] = {};
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_decode_static_scratch[kStaticScratchBytes];
+
+extern "C" zp_status zp_paged_decode_attn_static(const zp_kv_pool* pool, int32_t layer, const uint16_t* q,
+                                                 const int32_t* block_tables, const int32_t* seq_lens,
+                                                 int32_t B, int32_t max_blocks, uint16_t* out,
+                                                 const zp_params* p, int32_t* dev_status, zp_stream stream) {
+  zp_status s = decode_validate(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p);
+  if (s != ZP_OK) return s;
+  const size_t need = zp_paged_decode_workspace_size(p, B, max_blocks) - 256;  // partials only
+  if (need > kStaticScratchBytes - kStaticErrBytes) return ZP_ERR_TOO_LARGE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevicesStatic) return ZP_ERR_UNSUPPORTED;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_decode_static_scratch) != cudaSuccess || !addr) return ZP_ERR_CUDA;
+      g_static_addr[dev] = addr;
+    }
+    base = g_static_addr[dev];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* err = dev_status ? dev_status : static_cast<int32_t*>(base);
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), st) != cudaSuccess) return ZP_ERR_CUDA;
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + kStaticErrBytes);
+  return decode_launch(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p, part, err, st);
 }

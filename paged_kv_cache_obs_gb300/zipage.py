@@ -21,8 +21,9 @@ ZP_ERR_BAD_TABLE = 3
 ZP_ERR_TIMEOUT = 4
 ZP_ERR_CUDA = 5
 ZP_ERR_UNSUPPORTED = 6
+ZP_ERR_TOO_LARGE = 7
 _NAMES = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_NO_BLOCKS", 3: "ZP_ERR_BAD_TABLE",
-          4: "ZP_ERR_TIMEOUT", 5: "ZP_ERR_CUDA", 6: "ZP_ERR_UNSUPPORTED"}
+          4: "ZP_ERR_TIMEOUT", 5: "ZP_ERR_CUDA", 6: "ZP_ERR_UNSUPPORTED", 7: "ZP_ERR_TOO_LARGE"}
 
 
 class ZipageError(RuntimeError):
@@ -81,6 +82,8 @@ _sig("zp_compress_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32])
 _sig("zp_paged_decode_attn", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                     ctypes.POINTER(zp_params), _P, _SZ, _P])
 _sig("zp_paged_decode_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
+_sig("zp_paged_decode_attn_static", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
+                                           ctypes.POINTER(zp_params), _P, _P])
 _sig("zp_read_error", _I32, [_P, _P, _I32P])
 _sig("zp_alloc_create", _I32, [_I64, ctypes.POINTER(_P)])
 _sig("zp_alloc_destroy", None, [_P])
@@ -165,6 +168,18 @@ def zp_paged_decode_attn(pool, layer: int, q, block_tables, seq_lens, out, param
                                   ctypes.byref(make_params(params)), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream))
     _check("zp_paged_decode_attn", st)
+
+
+def zp_paged_decode_attn_static(pool, layer: int, q, block_tables, seq_lens, out, params: dict,
+                                dev_status=None, stream=None):
+    """Decode attention whose scratch is the library's fixed device array: nothing is
+    allocated, so callers without a device allocator can use it (see include/zipage.h).
+    dev_status: optional device int32 tensor receiving the device-side status."""
+    kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    st = lib.zp_paged_decode_attn_static(ctypes.byref(kv), layer, _ptr(q), _ptr(block_tables), _ptr(seq_lens),
+                                         q.shape[0], block_tables.shape[1], _ptr(out),
+                                         ctypes.byref(make_params(params)), _ptr(dev_status), _stream(stream))
+    _check("zp_paged_decode_attn_static", st)
 
 
 def zp_read_error(workspace, stream=None) -> int:
