@@ -386,6 +386,76 @@ def run_cpu_baseline(inp, pool, gs):
 
 # ------------------------------------------------------------------ reference arm -----------
 
+def run_mixed(args):
+    """Mixed serving step: the slot holders compress on a side stream while decode attention
+    (one new token, every layer) runs for the other requests on the main stream.  Reports the
+    compression alone, the decode alone, both concurrently, and the overlap they achieve."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_obs_gb300 import runner, synth, zipage
+    torch.cuda.set_device(0)
+    wl = workload_of(args)
+    inp = synth.make_inputs(wl, "cuda")
+    R = inp.num_compress
+    pristine = inp.pool.clone()
+    gs0 = inp.global_scores.clone()
+    batch = runner.CompressionBatch(inp, "cuda", pool=inp.pool)
+    p = wl.params()
+    nd = wl.num_decode
+    dec_tables = torch.from_numpy(np.ascontiguousarray(inp.block_tables[R:])).cuda()
+    dec_seq = torch.from_numpy(np.ascontiguousarray(inp.seq_len[R:])).cuda()
+    outs = torch.empty((wl.num_layers, nd, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, nd, wl.n_max))
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def compress():
+        batch.launch(stream=side)
+
+    def decode():
+        for l in range(wl.num_layers):
+            zipage.zp_paged_decode_attn(batch.pool, l, inp.decode_q[l], dec_tables, dec_seq, outs[l], p, ws,
+                                        stream=main)
+
+    def timed(fn_c, fn_d):
+        batch.pool.copy_(pristine)
+        batch.gs.copy_(gs0)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        ec, ed = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        side.wait_event(e0)
+        if fn_c:
+            fn_c()
+        ec.record(side)
+        if fn_d:
+            fn_d()
+        ed.record(main)
+        torch.cuda.synchronize()
+        return max(e0.elapsed_time(ec), e0.elapsed_time(ed))
+
+    for _ in range(args.warmup):
+        timed(compress, decode)
+    tc = np.median([timed(compress, None) for _ in range(args.steps)])
+    td = np.median([timed(None, decode) for _ in range(args.steps)])
+    tb = np.median([timed(compress, decode) for _ in range(args.steps)])
+    assert batch.error(side) == 0 and zipage.zp_read_error(ws, main) == 0
+    dec_tokens = int(inp.seq_len[R:].sum())
+    dec_bytes = dec_tokens * wl.num_kv_heads * wl.head_dim * 2 * 2 * wl.num_layers
+    out = {"metric": METRIC, "value": R * wl.num_layers / (tb / 1e3), "unit": "compressions/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": tb,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded)",
+           "config": {"workload": f"mixed: {R} compressing + {nd} decoding requests, {wl.num_layers} layers, "
+                                  f"pool {inp.pool.shape[1]} blocks",
+                      "note": "one step = compression pass on a side stream + decode of every layer on the main stream"},
+           "mixed": {"compress_ms": tc, "decode_ms": td, "both_ms": tb,
+                     "overlap_frac": (tc + td - tb) / min(tc, td),
+                     "decode_hbm_gbs": dec_bytes / (td / 1e3) / 1e9, "decode_tokens_per_layer": dec_tokens},
+           "gpu_launches": 1 + 2 * wl.num_layers}
+    print(json.dumps(out), flush=True)
+    batch.close()
+
+
 def workload_of(args):
     from paged_kv_cache_obs_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
@@ -441,6 +511,8 @@ def main(argv=None):
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "mixed":
+        run_mixed(args)
     else:
         run_ours(args)
 

@@ -28,6 +28,7 @@
 //      from shared memory, V rows from registers, G' from registers.
 // All waits are bounded; a failed wait or a bad table makes the whole unit skip its writes.
 #include <cstdio>
+#include <algorithm>
 #include <mutex>
 
 #include "zp_internal.h"
@@ -54,6 +55,7 @@ struct CompressArgs {
   const int32_t* qslot;
   float* gscores;
   int32_t* err;
+  int32_t* work;                    // unit counter of the persistent clusters (zeroed per launch)
   float* dbg_attn;
   float* dbg_redund;
   float* dbg_score;
@@ -64,6 +66,7 @@ struct CompressArgs {
   uint32_t block_bytes;           // bytes of one (layer, block): 2 * Hkv * b * d * 2
   uint32_t kv_bytes;              // bytes of the K (or V) part of a block: Hkv * b * d * 2
   uint32_t row_bytes;             // d * 2
+  int b_shift;                    // log2(b)
   int protect_window, causal;
 };
 
@@ -72,7 +75,8 @@ struct __align__(1024) Smem {
   uint8_t Q[2][kRows * 128];
   union {
     float2 part[2][kRows];          // pass-1 (max, sum) per column half
-    float norm[kKeysPerCta];        // key norms (Gram diagonal)
+    float norm[kKeysPerCta];        // reciprocal key norms (Gram diagonal)
+    unsigned long long lists[192];  // cluster-level merge of the eviction candidates
   } u0;
   union {
     float2 recv[kMaxCluster][kRows];            // (max, sum) partials of every CTA
@@ -81,7 +85,7 @@ struct __align__(1024) Smem {
       unsigned long long wcand[kKeysPerCta];    // per-warp candidates
     } sel;
   } u1;
-  unsigned long long cand_recv[kMaxCluster * kMaxEvict];  // [cta * E + rank]
+  unsigned long long cand_recv[kMaxCluster * 32];  // sorted bottom-32 list of every CTA
   int status_recv[kMaxCluster];
   float row_off[kRows];
   int evict_pos[kMaxEvict];
@@ -92,6 +96,7 @@ struct __align__(1024) Smem {
   uint64_t bar_mma;
   uint64_t bar_v;
   uint32_t tmem_base;
+  int next_unit[2];                 // unit after the current one, pushed by cluster rank 0
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -118,6 +123,36 @@ __device__ __forceinline__ unsigned long long evict_key(float s, int t) {
   return (static_cast<unsigned long long>(order_bits(s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(t));
 }
 
+// Sorts one 64-bit key per lane ascending across the warp (bitonic network).
+__device__ __forceinline__ unsigned long long warp_sort32(unsigned long long x, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+      const bool take_min = ((lane & j) == 0) == ((lane & k) == 0);
+      const unsigned long long lo = x < y ? x : y, hi = x < y ? y : x;
+      x = take_min ? lo : hi;
+    }
+  }
+  return x;
+}
+
+// The 32 smallest of two ascending 32-key lists (one key per lane each), ascending: the
+// elementwise minimum of a and reversed b is bitonic and holds them; a bitonic merge sorts it.
+__device__ __forceinline__ unsigned long long warp_merge_low32(unsigned long long a, unsigned long long b,
+                                                               int lane) {
+  const unsigned long long br = __shfl_sync(0xffffffffu, b, 31 - lane);
+  unsigned long long x = a < br ? a : br;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+    const unsigned long long lo = x < y ? x : y, hi = x < y ? y : x;
+    x = ((lane & j) == 0) ? lo : hi;
+  }
+  return x;
+}
+
 __device__ __forceinline__ void record_error(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -138,17 +173,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int q4 = warp & 3, hh = warp >> 2;  // TMEM lane quarter, key/column half
   const int C = static_cast<int>(cluster_nctarank());
   const int c = static_cast<int>(cluster_ctarank());
-  const int h = blockIdx.y;
-  const int r = blockIdx.z / a.layers;
-  const int layer = blockIdx.z % a.layers;
   const int L = a.L, b = a.b, d = a.d, w = a.w, Rw = a.Rw, Gq = a.Gq;
+  const int bs = a.b_shift, bm = b - 1;  // b is a power of two: t / b = t >> bs, t % b = t & bm
   const int t0 = c * kKeysPerCta;
   const int nk = min(kKeysPerCta, L - t0);
   const int nhalf = d / 64;
-  uint8_t* const head_base = a.pool + static_cast<size_t>(layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
-                             static_cast<size_t>(h) * b * a.row_bytes;
+  const int num_units = a.R * a.layers * a.Hkv;
+  const int cluster_id = static_cast<int>(blockIdx.x) / C;  // the C CTAs of a cluster are consecutive in x
+  const int num_clusters = static_cast<int>(gridDim.x) / C;
 
-  // ---------------------------------------------------------------- set-up --------------
+  // ---------------------------------------------------------------- once per CTA --------
   if (tid == 0) {
     mbar_init(&s.bar_tma, 1);
     mbar_init(&s.bar_mma, 1);
@@ -159,10 +193,55 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncwarp();
   if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  // mbarrier phases, tracked by the waiting thread (tid 0): every unit completes bar_tma once,
+  // bar_v once (unless skipped) and bar_mma three times (unless skipped)
+  uint32_t ph_tma = 0, ph_mma = 0, ph_v = 0;
+
+  // Persistent clusters: cluster i starts with unit i and then takes the next unused unit from
+  // a global counter (fetched by cluster rank 0, broadcast through shared memory); a unit is
+  // (request, layer, kv head) with the kv head fastest.
+  int iter = 0;
+  for (int unit = cluster_id; unit < num_units; ++iter) {
+  const int h = unit % a.Hkv;
+  const int r = unit / a.Hkv / a.layers;
+  const int layer = (unit / a.Hkv) % a.layers;
+  uint8_t* const head_base = a.pool + static_cast<size_t>(layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
+                             static_cast<size_t>(h) * b * a.row_bytes;
+
+  // ---- set-up of the unit.  Thread 0 issues the TMA of K and Q straight away from the table
+  //      entries it reads itself; a block id outside the pool only makes TMA fill zeros, and
+  //      the unit is then skipped after validation below (waiting for the copies).
+  const int slot = a.qslot[r];
+  bool tma_pending = false, v_pending = false;  // (tid 0) copies issued and not yet waited for
+  if (warp == 0) {
+    // lane 0 registers the bytes, then every lane issues the boxes of its own block(s)
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nk + Rw) * d * 2));
+      for (int hd = 0; hd < nhalf; ++hd)
+        tma_load_3d(&s.Q[hd][0], &tmQ, &s.bar_tma, hd * 64, h * Gq, (slot * a.layers + layer) * w);
+      tma_pending = true;
+    }
+    __syncwarp();
+    const int32_t* trow = a.block_tables + static_cast<int64_t>(r) * a.max_blocks + (t0 >> bs);
+    for (int bi = lane; bi < (nk >> bs); bi += 32) {
+      const int phys = trow[bi];
+      for (int hd = 0; hd < nhalf; ++hd)
+        tma_load_3d(&s.K[hd][bi * b * 128], &tmK, &s.bar_tma, hd * 64, h * b,
+                    layer * static_cast<int>(a.num_blocks) + phys);
+    }
+    __syncwarp();
+  }
+  // cluster rank 0 fetches the unit after this one now and sends it to every CTA with its
+  // status before barrier #2 (the atomic's latency overlaps the unit's work)
+  int next_fetch = 0;
+  if (c == 0 && tid == 0) next_fetch = num_clusters + atomicAdd(a.work, 1);
 
   // Validate the request's metadata; every CTA of the cluster sees the same values, so they
   // all take the same decision without communicating.
-  const int slot = a.qslot[r];
   bool bad = (a.seq_len[r] != L) || slot < 0 || slot >= a.num_qslots;
   for (int i = tid; i < a.n_max; i += kThreads) {
     const int sb = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + i];
@@ -171,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     s.dst_tab[i] = db;
     bad |= (sb < 0 || sb >= a.num_blocks || db < 0 || db >= a.num_blocks);
   }
-  // Zero the padding rows of Q (never touched by the TMA box).
+  // Zero the padding rows of Q (never touched by the TMA box; the V staging of the previous
+  // unit may have used them).
   for (int i = Rw * 8 + tid; i < kRows * 8; i += kThreads) {
     const int row = i >> 3, ch = i & 7;
     reinterpret_cast<uint4*>(s.Q[0])[row * 8 + ch] = make_uint4(0, 0, 0, 0);
@@ -182,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool skip = __syncthreads_or(bad);
   tc_fence_after();
   if (skip && tid == 0 && c == 0) record_error(a.err, ZP_ERR_BAD_TABLE);
-  const uint32_t tbase = s.tmem_base;
 
   const int kt = t0 + tid;  // the key this thread owns from pass 2 on
   const bool key_valid = tid < nk;
@@ -195,17 +274,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!skip) {
     if (key_valid) g_in = a.gscores[((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L + kt];
     if (tid == 0) {
-      mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nk + Rw) * d * 2));
-      for (int hd = 0; hd < nhalf; ++hd)
-        tma_load_3d(&s.Q[hd][0], &tmQ, &s.bar_tma, hd * 64, h * Gq, (slot * a.layers + layer) * w);
-      const int nblk = nk / b;
-      for (int bi = 0; bi < nblk; ++bi) {
-        const int phys = s.src_tab[t0 / b + bi];
-        for (int hd = 0; hd < nhalf; ++hd)
-          tma_load_3d(&s.K[hd][bi * b * 128], &tmK, &s.bar_tma, hd * 64, h * b,
-                      layer * static_cast<int>(a.num_blocks) + phys);
+      ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
+      if (ok) {
+        ph_tma ^= 1;
+        tma_pending = false;
       }
-      ok = mbar_wait_bounded(&s.bar_tma, 0, kWaitNs);
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(128, nk);
       for (int kk = 0; kk < d / 16; ++kk) {
@@ -214,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_bf16(tbase, ad, bd, idesc, kk > 0);
       }
       mma_commit(&s.bar_mma);
-      ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
+      ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
+      ph_mma ^= 1;
     }
   }
   bool fail = __syncthreads_or(!ok);
@@ -325,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       s.row_off[tid] = (tid < Rw && Lsum > 0.0f) ? fmaf(M, a.sl2, lg2(Lsum)) : INFINITY;
     }
-    if (tid == 0) ok = mbar_wait_bounded(&s.bar_mma, 1, kWaitNs) && ok;
+    if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
+      ph_mma ^= 1;
+    }
   }
   fail |= __syncthreads_or(!ok);
   tc_fence_after();
@@ -361,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_commit(&s.bar_mma);
     }
     if (key_valid) {
-      const int jb0 = (tid & 31) / b * b;  // first column of this key's block within gv
+      const int jb0 = (tid & 31) & ~bm;  // first column of this key's block within gv
       const float4* inv4 = reinterpret_cast<const float4*>(&s.u0.norm[tid & ~31]);
       float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
@@ -377,7 +454,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       red = (acc0 + acc1) * inv_nt * a.inv_bm1;
     }
-    if (tid == 0) ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
+    if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
+      ph_mma ^= 1;
+    }
   }
   fail |= __syncthreads_or(!ok);
   tc_fence_after();
@@ -390,11 +470,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int nv0 = min(128, nk);
   if (!skip && tid == 0) {
     mbar_arrive_expect_tx(&s.bar_v, static_cast<uint32_t>(nv0) * a.row_bytes);
-    for (int bi = 0; bi < nv0 / b; ++bi) {
-      const uint8_t* src = head_base + row_off_bytes(a, s.src_tab[t0 / b + bi], 1, 0);
+    for (int bi = 0; bi < (nv0 >> bs); ++bi) {
+      const uint8_t* src = head_base + row_off_bytes(a, s.src_tab[(t0 >> bs) + bi], 1, 0);
       bulk_load(vstage + static_cast<size_t>(bi) * b * a.row_bytes, src, static_cast<uint32_t>(b) * a.row_bytes,
                 &s.bar_v);
     }
+    v_pending = true;
   }
   __syncwarp();  // warp 0 reconverges before the collective TMEM loads
   if (!skip) {
@@ -446,64 +527,70 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row = 128 + warp * 16 + it * rpi + lane / cpr, ch = lane % cpr;
     if (!skip && it * rpi < 16 && row < nk) {
       const int t = t0 + row;
-      vreg[it] = *reinterpret_cast<const uint4*>(head_base + row_off_bytes(a, s.src_tab[t / b], 1, t % b) + ch * 16);
+      vreg[it] = *reinterpret_cast<const uint4*>(head_base + row_off_bytes(a, s.src_tab[t >> bs], 1, t & bm) + ch * 16);
     }
   }
 
-  // ---- step 6: selection, level 1: per-warp bottom-E by rank counting over the warp's keys
+  // ---- step 6: selection.  The E evicted keys are the E smallest eviction keys of the
+  //      cluster.  Each warp sorts its 32 keys; the 8 sorted lists merge pairwise (bottom 32
+  //      of each pair) in a 3-level tree; the CTA's sorted bottom 32 go to every CTA.
+  unsigned long long* const lst = s.u1.sel.key;   // [8][32] sorted lists, reused per level
+  unsigned long long* const lst2 = s.u1.sel.wcand;
   if (!skip) {
-    const int E = a.E;
     const unsigned long long mykey = key_valid ? evict_key(S, kt) : (~0ull - static_cast<unsigned long long>(tid));
-    int wr = 0;
-#pragma unroll
-    for (int u = 0; u < 32; ++u) wr += (__shfl_sync(0xffffffffu, mykey, u) < mykey) ? 1 : 0;
-    const int wE = min(E, 32);
-    if (wr < wE) s.u1.sel.wcand[warp * wE + wr] = mykey;
+    lst[warp * 32 + lane] = warp_sort32(mykey, lane);
   }
   __syncthreads();
-
+  if (!skip && (warp & 1) == 0)
+    lst[warp * 32 + lane] = warp_merge_low32(lst[warp * 32 + lane], lst[(warp + 1) * 32 + lane], lane);
+  __syncthreads();
+  if (!skip && (warp & 3) == 0)
+    lst[warp * 32 + lane] = warp_merge_low32(lst[warp * 32 + lane], lst[(warp + 2) * 32 + lane], lane);
+  __syncthreads();
   if (!skip) {
-    // level 2: rank each warp candidate among all of this CTA's warp candidates
-    const int E = a.E;
-    const int ncand = (kThreads / 32) * min(E, 32);
-    if (tid < ncand) {
-      const unsigned long long key = s.u1.sel.wcand[tid];
-      const ulonglong2* w2 = reinterpret_cast<const ulonglong2*>(s.u1.sel.wcand);
-      int rk = 0;
-#pragma unroll 4
-      for (int u = 0; u < ncand / 2; ++u) {
-        const ulonglong2 kk = w2[u];
-        rk += (kk.x < key) + (kk.y < key);
-      }
-      if (rk < E) {
-        const uint32_t local = smem_u32(&s.cand_recv[c * E + rk]);
-        for (int dst = 0; dst < C; ++dst) st_cluster_u64(mapa(local, dst), key);
-      }
+    if (warp == 0) {
+      const unsigned long long mine = warp_merge_low32(lst[lane], lst[4 * 32 + lane], lane);
+      const uint32_t local = smem_u32(&s.cand_recv[c * 32 + lane]);
+      for (int dst = 0; dst < C; ++dst) st_cluster_u64(mapa(local, dst), mine);
     }
     if (tid == 0) {
-      ok = mbar_wait_bounded(&s.bar_v, 0, kWaitNs) && ok;  // staged V rows have landed
+      const bool vok = mbar_wait_bounded(&s.bar_v, ph_v, kWaitNs);  // staged V rows have landed
+      if (vok) {
+        ph_v ^= 1;
+        v_pending = false;
+      }
+      ok = ok && vok;
       const uint32_t local = smem_u32(&s.status_recv[c]);
       for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), (fail || !ok) ? 1u : 0u);
     }
   }
+  if (c == 0 && tid == 0) {  // the next unit reaches every CTA with this barrier, skipped or not
+    const uint32_t nl = smem_u32(&s.next_unit[iter & 1]);
+    for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(nl, dst), static_cast<uint32_t>(next_fetch));
+  }
   cluster_sync();  // #2: candidates, statuses and every read of every CTA of the unit are done
+  const int next_unit = s.next_unit[iter & 1];
 
   bool any_fail = false;
   if (!skip) {
     for (int cc = 0; cc < C; ++cc) any_fail |= s.status_recv[cc] != 0;
     const int E = a.E;
-    const int ntot = C * E;
-    // level 3: the E lowest keys of the cluster, identical in every CTA
-    if (tid < ntot) {
-      const unsigned long long key = s.cand_recv[tid];
-      const ulonglong2* c2v = reinterpret_cast<const ulonglong2*>(s.cand_recv);
-      int rk = 0;
-#pragma unroll 4
-      for (int u = 0; u < ntot / 2; ++u) {
-        const ulonglong2 kk = c2v[u];
-        rk += (kk.x < key) + (kk.y < key);
-      }
-      if (rk < E) s.evict_pos[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
+    // cluster level: merge the C sorted lists (missing lists count as +inf), identically in
+    // every CTA; the first E keys of the result are evicted
+    // scratch in u0: the u1 buffers may already receive the next unit's row statistics
+    unsigned long long* const m4 = s.u0.lists;       // [4][32]
+    unsigned long long* const m2 = s.u0.lists + 128; // [2][32]
+    if (warp < 4) {
+      const unsigned long long x0 = (2 * warp < C) ? s.cand_recv[(2 * warp) * 32 + lane] : ~0ull;
+      const unsigned long long x1 = (2 * warp + 1 < C) ? s.cand_recv[(2 * warp + 1) * 32 + lane] : ~0ull;
+      m4[warp * 32 + lane] = warp_merge_low32(x0, x1, lane);
+    }
+    __syncthreads();
+    if (warp < 2) m2[warp * 32 + lane] = warp_merge_low32(m4[(2 * warp) * 32 + lane], m4[(2 * warp + 1) * 32 + lane], lane);
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned long long fin = warp_merge_low32(m2[lane], m2[32 + lane], lane);
+      if (lane < E) s.evict_pos[lane] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(fin & 0xFFFFFFFFu));
     }
     __syncthreads();
 
@@ -524,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (a.dbg_keep)
         a.dbg_keep[((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt] = evicted ? 0 : 1;
     }
-    const bool moved = j >= 0 && (s.src_tab[kt / b] != s.dst_tab[j / b] || kt % b != j % b);
+    const bool moved = j >= 0 && (s.src_tab[kt >> bs] != s.dst_tab[j >> bs] || (kt & bm) != (j & bm));
     s.dst_of[tid] = moved ? j : -1;
     __syncthreads();
 
@@ -544,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (jj < 0) continue;
           const uint4 kv = *reinterpret_cast<const uint4*>(&s.K[half][row * 128 + ((c8 ^ (row & 7)) << 4)]);
           const uint4 vv = part == 0 ? *reinterpret_cast<const uint4*>(vstage + row * a.row_bytes + ch * 16) : vreg[it];
-          uint8_t* dk = head_base + row_off_bytes(a, s.dst_tab[jj / b], 0, jj % b) + ch * 16;
+          uint8_t* dk = head_base + row_off_bytes(a, s.dst_tab[jj >> bs], 0, jj & bm) + ch * 16;
           *reinterpret_cast<uint4*>(dk) = kv;
           *reinterpret_cast<uint4*>(dk + a.kv_bytes) = vv;
         }
@@ -555,10 +642,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   if (!skip && any_fail && tid == 0 && c == 0) record_error(a.err, ZP_ERR_TIMEOUT);
-
+  // copies a skipped or failed unit issued and never saw complete: wait (bounded) before the
+  // shared memory is reused
+  if (tid == 0) {
+    if (tma_pending && mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs)) ph_tma ^= 1;
+    if (v_pending && mbar_wait_bounded(&s.bar_v, ph_v, kWaitNs)) ph_v ^= 1;
+  }
+  // every generic read of K / the staging area and every TMEM load of this unit precedes the
+  // next unit's TMA and MMAs
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  unit = next_unit;
+  }  // unit loop
+
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
@@ -570,7 +668,7 @@ size_t compress_smem_bytes() { return sizeof(Smem) + 1024; }
 
 using namespace zp;
 
-extern "C" size_t zp_compress_workspace_size(const zp_params*, int32_t) { return 256; }
+extern "C" size_t zp_compress_workspace_size(const zp_params*, int32_t) { return 256; }  // error word + unit counter
 
 extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
                                  const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
@@ -596,11 +694,11 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   if (Gq > 256 || w > 256) return ZP_ERR_UNSUPPORTED;
   if (!aligned(pool->base, 16) || !aligned(obs_q, 16)) return ZP_ERR_INVALID_ARG;
   if (static_cast<int64_t>(layers) * pool->num_blocks >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(R) * layers > 65535) return ZP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(R) * layers * Hkv >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(num_qslots) * layers * w >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 4, st) != cudaSuccess) return ZP_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 8, st) != cudaSuccess) return ZP_ERR_CUDA;  // error word, unit counter
   if (R == 0) return ZP_OK;
 
   CUtensorMap tmK, tmQ;
@@ -624,6 +722,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.qslot = meta->qslot;
   a.gscores = global_scores;
   a.err = static_cast<int32_t*>(workspace);
+  a.work = static_cast<int32_t*>(workspace) + 1;
   if (dbg) {
     a.dbg_attn = dbg->attn;
     a.dbg_redund = dbg->redund;
@@ -652,6 +751,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.inv_rw = 1.0f / static_cast<float>(Rw);
   a.inv_bm1 = 1.0f / static_cast<float>(b - 1);
   a.row_bytes = static_cast<uint32_t>(d) * 2;
+  a.b_shift = (b == 16) ? 4 : 5;
   a.kv_bytes = static_cast<uint32_t>(Hkv) * b * a.row_bytes;
   a.block_bytes = 2 * a.kv_bytes;
   a.protect_window = p->protect_window;
@@ -667,8 +767,9 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
 
   const int C = (L + kKeysPerCta - 1) / kKeysPerCta;
+  const int64_t num_units = static_cast<int64_t>(R) * layers * Hkv;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(C, Hkv, R * layers);
+  cfg.gridDim = dim3(C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -679,6 +780,27 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // as many clusters as are co-resident (persistent), never more than there are units
+  static std::mutex occ_mu;
+  static int occ_cache[64][kMaxCluster + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZP_ERR_CUDA;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(occ_mu);
+    if (dev >= 0 && dev < 64 && occ_cache[dev][C] > 0) {
+      max_clusters = occ_cache[dev][C];
+    } else {
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, compress_kernel, &cfg) != cudaSuccess || max_clusters <= 0)
+        max_clusters = 1;
+      if (dev >= 0 && dev < 64) occ_cache[dev][C] = max_clusters;
+    }
+  }
+  // Units are handed out dynamically, so launching more clusters than can be resident only
+  // leaves the late ones an empty queue; two CTAs fit per SM.
+  const int64_t want = std::max<int64_t>(max_clusters, (2 * static_cast<int64_t>(num_sms())) / C);
+  const int64_t clusters = std::min<int64_t>(num_units, want);
+  cfg.gridDim = dim3(static_cast<unsigned>(C * clusters), 1, 1);
   if (cudaLaunchKernelEx(&cfg, compress_kernel, tmK, tmQ, a) != cudaSuccess) return ZP_ERR_CUDA;
   return ZP_OK;
 }
