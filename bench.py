@@ -131,23 +131,24 @@ def algorithmic_bytes(batch, keep):
     """
     import torch
     wl = batch.wl
-    R, nl, Hkv, d, b, L, w = (batch.inp.num_compress, wl.num_layers, wl.num_kv_heads, wl.head_dim,
-                              wl.block_size, wl.L, wl.window)
+    R, nl, Hkv, d, b, w = (batch.inp.num_compress, wl.num_layers, wl.num_kv_heads, wl.head_dim,
+                           wl.block_size, wl.window)
     Gq = wl.num_q_heads // Hkv
-    heads = R * nl * Hkv
     dev = keep.device
-    t = torch.arange(L, device=dev)
     moved_total = 0
+    total = 0
     for r in range(R):
-        kp = keep[r].to(torch.int64)                           # [nl, Hkv, L]
+        L = int(batch.seq_len[r])
+        t = torch.arange(L, device=dev)
+        kp = keep[r, :, :, :L].to(torch.int64)                 # [nl, Hkv, L]
         j = torch.cumsum(kp, -1) - 1                           # destination slot of kept t
         src_tab = torch.from_numpy(batch.tables[r]).to(dev).long()
         dst_tab = torch.from_numpy(batch.dst_tables[r]).to(dev).long()
         jj = j.clamp(min=0)
         same = (src_tab[t // b][None, None, :] == dst_tab[jj // b]) & ((t % b)[None, None, :] == jj % b)
         moved_total += int(((kp == 1) & ~same).sum().item())
-    per_head_fixed = L * d * 2 + w * Gq * d * 2 + 2 * L * 4
-    total = heads * per_head_fixed + moved_total * 3 * d * 2 + R * nl * 2 * wl.n_max * 4
+        total += nl * Hkv * (L * d * 2 + w * Gq * d * 2 + 2 * L * 4) + nl * 2 * ((L + b - 1) // b) * 4
+    total += moved_total * 3 * d * 2
     return total, moved_total
 
 

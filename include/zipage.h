@@ -77,14 +77,19 @@ typedef struct zp_kv_pool {
 
 typedef struct zp_seq_meta {
   int32_t num_requests;       /* R: requests compressed by this call */
-  int32_t max_blocks;         /* row stride of the block tables (>= n_max) */
-  const int32_t* seq_len;     /* device [R]: cached tokens; must equal n_max*b */
+  int32_t max_blocks;         /* row stride of the block tables (>= ceil(L_max / b)) */
+  const int32_t* seq_len;     /* device [R]: cached tokens L of each request, k < L <= L_max
+                                 (L = n_max*b at the decode trigger; a request that left a long
+                                 prefill may hold more, zh §2.1) */
   const int32_t* qslot;       /* device [R]: query slot of each request, 0 <= qslot < num_qslots */
   const int32_t* dst_tables;  /* device [R][max_blocks]: where survivors go; equals the source
                                  table except at target blocks (zp_plan_compress) */
+  int32_t max_seq_len;        /* L_max: the longest seq_len of the call (<= 2048), or 0 for
+                                 n_max*b.  It is also the row length of global_scores and of
+                                 the zp_debug arrays. */
 } zp_seq_meta;
 
-/* Optional per-token outputs, each device [R][num_layers][num_kv_heads][n_max*b] (row-major),
+/* Optional per-token outputs, each device [R][num_layers][num_kv_heads][L_max] (row-major),
  * any field may be NULL.  attn = window attention score, redund = Lightning redundancy,
  * score = combined score S (+inf on protected tokens), keep = 1 if kept else 0. */
 typedef struct zp_debug {
@@ -98,7 +103,7 @@ typedef struct zp_debug {
  * Compression pass (zh §2.1 core mechanism; zh §2.3 cross-layer parallel compression).
  *
  * One launch covers every (request, layer, kv head) unit.  For unit (r, l, h) with
- * L = n_max*b cached tokens read through block_tables[r]:
+ * L = seq_len[r] cached tokens read through block_tables[r]:
  *   attn[t]  = mean over the w*G_q window rows (i, g) of softmax_t(scale*<q_{i,g}, k_t>),
  *              row i being the query of position L-w+i (causal if params.causal);
  *   R[t]     = mean cosine similarity of k_t to the other keys of its block (Lightning);
@@ -113,7 +118,7 @@ typedef struct zp_debug {
  *   obs_q         device bf16 [num_qslots][num_layers][w][H_q][d]: the window queries;
  *                 16-byte aligned.
  *   num_qslots    M, number of query slots in obs_q and global_scores.
- *   global_scores device fp32 [num_qslots][num_layers][H_kv][n_max*b], updated in place.
+ *   global_scores device fp32 [num_qslots][num_layers][H_kv][L_max], updated in place.
  *   params        host.
  *   dbg           host struct or NULL.
  *   workspace     device, >= zp_compress_workspace_size() bytes, 256-byte aligned; holds the
@@ -221,10 +226,13 @@ zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, i
                            int32_t n_max, int32_t* host_dst_tables);
 
 /* After the compression launched on `stream`: for each request, decref every replaced shared
- * block (old != new for i < n_max-1) and the old last block old[n_max-1], deferred until the
- * work queued on `stream` has finished (the kernel still reads those blocks). */
+ * block (old != new for i < n_max-1) and every old block past the first n_max-1
+ * (old[n_max-1 .. ceil(seq_len/b)) — the last block at the decode trigger, more after a
+ * prefill), deferred until the work queued on `stream` has finished (the kernel still reads
+ * those blocks).  host_seq_len: host [R], or NULL when every request holds n_max blocks. */
 zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables,
-                             int32_t R, int32_t max_blocks, int32_t n_max, zp_stream stream);
+                             int32_t R, int32_t max_blocks, int32_t n_max, int32_t block_size,
+                             const int32_t* host_seq_len, zp_stream stream);
 
 /* Library version, for the binding's sanity check. */
 int32_t zp_version(void);

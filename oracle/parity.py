@@ -91,14 +91,14 @@ def check_units(units, pool_in, obs_q, gs_in, tables, dst_tables, seq_len, qslot
     for (r, l, h) in units:
         u = ref[(r, l, h)]
         where = f" at unit (r={r}, layer={l}, h={h})"
-        assert_close("attn", dbg_gpu["attn"][r, l, h], u["attn"], where)
-        assert_close("redundancy", dbg_gpu["redund"][r, l, h], u["R"], where)
-        assert_close("score", dbg_gpu["score"][r, l, h], u["S"], where)
-        src = check_selection(dbg_gpu["keep"][r, l, h], dbg_gpu["score"][r, l, h], u["S"], k, where)
+        L = int(seq_len[r])
+        assert_close("attn", dbg_gpu["attn"][r, l, h][:L], u["attn"], where)
+        assert_close("redundancy", dbg_gpu["redund"][r, l, h][:L], u["R"], where)
+        assert_close("score", dbg_gpu["score"][r, l, h][:L], u["S"], where)
+        src = check_selection(dbg_gpu["keep"][r, l, h][:L], dbg_gpu["score"][r, l, h][:L], u["S"], k, where)
         ndiff += len(np.setxor1d(src, u["src"]))
         srcs[(r, l, h)] = src
         s = int(qslot[r])
-        L = int(seq_len[r])
         g_want = O.global_update(gs_in[s, l, h, :L].astype(np.float64), u["attn"], src, params["decay"], L)
         assert_close("global score", gs_out[s, l, h, :k], g_want[:k], where)
         assert (gs_out[s, l, h, k:L] == 0).all(), f"global-score tail not zero{where}"

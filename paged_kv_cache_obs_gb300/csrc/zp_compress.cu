@@ -60,9 +60,9 @@ struct CompressArgs {
   float* dbg_redund;
   float* dbg_score;
   int32_t* dbg_keep;
-  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, E, max_blocks, num_qslots;
+  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, max_blocks, num_qslots;  // L: launch length
   float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
-  float inv_rw, inv_bm1;          // 1 / (w * G_q), 1 / (b - 1)
+  float inv_rw;                   // 1 / (w * G_q)
   uint32_t block_bytes;           // bytes of one (layer, block): 2 * Hkv * b * d * 2
   uint32_t kv_bytes;              // bytes of the K (or V) part of a block: Hkv * b * d * 2
   uint32_t row_bytes;             // d * 2
@@ -97,6 +97,8 @@ struct __align__(1024) Smem {
   uint64_t bar_v;
   uint32_t tmem_base;
   int next_unit[2];                 // unit after the current one, pushed by cluster rank 0
+  int kept_recv[kMaxCluster];       // kept keys of every CTA (many-eviction path)
+  int warp_kept[kThreads / 32];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -173,10 +175,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int q4 = warp & 3, hh = warp >> 2;  // TMEM lane quarter, key/column half
   const int C = static_cast<int>(cluster_nctarank());
   const int c = static_cast<int>(cluster_ctarank());
-  const int L = a.L, b = a.b, d = a.d, w = a.w, Rw = a.Rw, Gq = a.Gq;
+  // La: the longest sequence of the launch (cluster size, TMA/MMA shapes, row length of the
+  // global scores); L: this unit's own sequence length (all masking and selection)
+  const int La = a.L, b = a.b, d = a.d, w = a.w, Rw = a.Rw, Gq = a.Gq;
   const int bs = a.b_shift, bm = b - 1;  // b is a power of two: t / b = t >> bs, t % b = t & bm
   const int t0 = c * kKeysPerCta;
-  const int nk = min(kKeysPerCta, L - t0);
+  const int nk_l = min(kKeysPerCta, La - t0);          // keys of this CTA at the launch length
+  const int nblk_l = (nk_l + bm) >> bs;                // blocks loaded (a partial last block whole)
+  const int n_mma = (nk_l + 15) & ~15;                 // MMA N over those keys
   const int nhalf = d / 64;
   const int num_units = a.R * a.layers * a.Hkv;
   const int cluster_id = static_cast<int>(blockIdx.x) / C;  // the C CTAs of a cluster are consecutive in x
@@ -220,14 +226,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) {
     // lane 0 registers the bytes, then every lane issues the boxes of its own block(s)
     if (lane == 0) {
-      mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nk + Rw) * d * 2));
+      mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>(((nblk_l << bs) + Rw) * d * 2));
       for (int hd = 0; hd < nhalf; ++hd)
         tma_load_3d(&s.Q[hd][0], &tmQ, &s.bar_tma, hd * 64, h * Gq, (slot * a.layers + layer) * w);
       tma_pending = true;
     }
     __syncwarp();
     const int32_t* trow = a.block_tables + static_cast<int64_t>(r) * a.max_blocks + (t0 >> bs);
-    for (int bi = lane; bi < (nk >> bs); bi += 32) {
+    for (int bi = lane; bi < nblk_l; bi += 32) {
       const int phys = trow[bi];
       for (int hd = 0; hd < nhalf; ++hd)
         tma_load_3d(&s.K[hd][bi * b * 128], &tmK, &s.bar_tma, hd * 64, h * b,
@@ -241,15 +247,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (c == 0 && tid == 0) next_fetch = num_clusters + atomicAdd(a.work, 1);
 
   // Validate the request's metadata; every CTA of the cluster sees the same values, so they
-  // all take the same decision without communicating.
-  bool bad = (a.seq_len[r] != L) || slot < 0 || slot >= a.num_qslots;
-  for (int i = tid; i < a.n_max; i += kThreads) {
+  // all take the same decision without communicating.  A request holds L cached tokens with
+  // k < L <= La (L = n_max*b at the decode trigger; more after a long prefill).
+  const int L = a.seq_len[r];
+  bool bad = (L <= a.k) || (L > La) || slot < 0 || slot >= a.num_qslots;
+  const int nblk_req = bad ? 0 : (L + bm) >> bs;
+  for (int i = tid; i < nblk_req; i += kThreads) {
     const int sb = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + i];
-    const int db = a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + i];
     s.src_tab[i] = sb;
-    s.dst_tab[i] = db;
-    bad |= (sb < 0 || sb >= a.num_blocks || db < 0 || db >= a.num_blocks);
+    bad |= (sb < 0 || sb >= a.num_blocks);
   }
+  for (int i = tid; i < a.n_max - 1; i += kThreads) {
+    const int db = a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + i];
+    s.dst_tab[i] = db;
+    bad |= (db < 0 || db >= a.num_blocks);
+  }
+  const int nk = max(0, min(kKeysPerCta, L - t0));   // this unit's keys in this CTA
+  const int E = L - a.k;                              // tokens to evict per head
   // Zero the padding rows of Q (never touched by the TMA box; the V staging of the previous
   // unit may have used them).
   for (int i = Rw * 8 + tid; i < kRows * 8; i += kThreads) {
@@ -272,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // ---- step 1: TMA of K and Q, then D1 = Q K^T (M = 128 window rows, N = nk keys).  Only
   //      thread 0 waits on the mbarriers; the others block on the CTA barrier below.
   if (!skip) {
-    if (key_valid) g_in = a.gscores[((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L + kt];
+    if (key_valid) g_in = a.gscores[((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * La + kt];
     if (tid == 0) {
       ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
       if (ok) {
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_pending = false;
       }
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, nk);
+      const uint32_t idesc = idesc_bf16_f32(128, n_mma);
       for (int kk = 0; kk < d / 16; ++kk) {
         const uint64_t ad = smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32]));
         const uint64_t bd = smem_desc_sw128(smem_u32(&s.K[kk >> 2][(kk & 3) * 32]));
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!skip) {
     if (tid == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
-      for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
+      for (int kh = 0; kh < 2 && kh * 128 < nk_l; ++kh)
         for (int kk = 0; kk < d / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32]));
           mma_bf16(tbase + kh * 128, ad, ad, idesc, kk > 0);
@@ -429,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // D2 = K Q^T per 128-key half into the same TMEM columns (Gram fully read)
     if (tid == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
-      for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
+      for (int kh = 0; kh < 2 && kh * 128 < nk_l; ++kh)
         for (int kk = 0; kk < d / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32]));
           const uint64_t bd = smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32]));
@@ -439,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (key_valid) {
       const int jb0 = (tid & 31) & ~bm;  // first column of this key's block within gv
+      const int jlim = min(jb0 + b, L - t0 - (tid & ~31));  // columns of the block that hold tokens
+      const int m = jlim - jb0;                             // tokens in this key's block
       const float4* inv4 = reinterpret_cast<const float4*>(&s.u0.norm[tid & ~31]);
       float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
@@ -448,11 +464,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = 4 * q + e;
-          const float cv = (j >= jb0 && j < jb0 + b && j != lane) ? gv[j] * nn[e] : 0.0f;
+          const float cv = (j >= jb0 && j < jlim && j != lane) ? gv[j] * nn[e] : 0.0f;
           if (e & 1) acc1 += cv; else acc0 += cv;
         }
       }
-      red = (acc0 + acc1) * inv_nt * a.inv_bm1;
+      red = m > 1 ? (acc0 + acc1) * inv_nt / static_cast<float>(m - 1) : 0.0f;
     }
     if (tid == 0) {
       ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
@@ -468,9 +484,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   //      read of the unit from every write.
   uint8_t* const vstage = &s.Q[0][0];
   const int nv0 = min(128, nk);
-  if (!skip && tid == 0) {
-    mbar_arrive_expect_tx(&s.bar_v, static_cast<uint32_t>(nv0) * a.row_bytes);
-    for (int bi = 0; bi < (nv0 >> bs); ++bi) {
+  if (!skip && tid == 0 && nv0 > 0) {
+    const int nvb = (nv0 + bm) >> bs;  // whole blocks (a partial last block is copied whole)
+    mbar_arrive_expect_tx(&s.bar_v, static_cast<uint32_t>(nvb << bs) * a.row_bytes);
+    for (int bi = 0; bi < nvb; ++bi) {
       const uint8_t* src = head_base + row_off_bytes(a, s.src_tab[(t0 >> bs) + bi], 1, 0);
       bulk_load(vstage + static_cast<size_t>(bi) * b * a.row_bytes, src, static_cast<uint32_t>(b) * a.row_bytes,
                 &s.bar_v);
@@ -512,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     S = (attn + a.alpha * g_in) - a.beta * red;
     if (a.protect_window && kt >= L - w) S = INFINITY;
     if (key_valid) {
-      const int64_t o = ((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt;
+      const int64_t o = ((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * La + kt;
       if (a.dbg_attn) a.dbg_attn[o] = attn;
       if (a.dbg_redund) a.dbg_redund[o] = red;
       if (a.dbg_score) a.dbg_score[o] = S;
@@ -532,37 +549,83 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ---- step 6: selection.  The E evicted keys are the E smallest eviction keys of the
-  //      cluster.  Each warp sorts its 32 keys; the 8 sorted lists merge pairwise (bottom 32
-  //      of each pair) in a 3-level tree; the CTA's sorted bottom 32 go to every CTA.
-  unsigned long long* const lst = s.u1.sel.key;   // [8][32] sorted lists, reused per level
-  unsigned long long* const lst2 = s.u1.sel.wcand;
-  if (!skip) {
-    const unsigned long long mykey = key_valid ? evict_key(S, kt) : (~0ull - static_cast<unsigned long long>(tid));
-    lst[warp * 32 + lane] = warp_sort32(mykey, lane);
-  }
-  __syncthreads();
-  if (!skip && (warp & 1) == 0)
-    lst[warp * 32 + lane] = warp_merge_low32(lst[warp * 32 + lane], lst[(warp + 1) * 32 + lane], lane);
-  __syncthreads();
-  if (!skip && (warp & 3) == 0)
-    lst[warp * 32 + lane] = warp_merge_low32(lst[warp * 32 + lane], lst[(warp + 2) * 32 + lane], lane);
-  __syncthreads();
-  if (!skip) {
-    if (warp == 0) {
+  //      cluster (E = L - k, the same in every CTA of the cluster).
+  unsigned long long* const lst = s.u1.sel.key;
+  const unsigned long long mykey =
+      (!skip && key_valid) ? evict_key(S, kt) : (~0ull - static_cast<unsigned long long>(tid));
+  bool evicted = false;
+  if (E <= 32) {
+    // Each warp sorts its 32 keys; the 8 sorted lists merge pairwise (bottom 32 of each pair)
+    // in a 3-level tree; the CTA's sorted bottom 32 go to every CTA.
+    if (!skip) lst[warp * 32 + lane] = warp_sort32(mykey, lane);
+    __syncthreads();
+    if (!skip && (warp & 1) == 0)
+      lst[warp * 32 + lane] = warp_merge_low32(lst[warp * 32 + lane], lst[(warp + 1) * 32 + lane], lane);
+    __syncthreads();
+    if (!skip && (warp & 3) == 0)
+      lst[warp * 32 + lane] = warp_merge_low32(lst[warp * 32 + lane], lst[(warp + 2) * 32 + lane], lane);
+    __syncthreads();
+    if (!skip && warp == 0) {
       const unsigned long long mine = warp_merge_low32(lst[lane], lst[4 * 32 + lane], lane);
       const uint32_t local = smem_u32(&s.cand_recv[c * 32 + lane]);
       for (int dst = 0; dst < C; ++dst) st_cluster_u64(mapa(local, dst), mine);
     }
-    if (tid == 0) {
-      const bool vok = mbar_wait_bounded(&s.bar_v, ph_v, kWaitNs);  // staged V rows have landed
+  } else {
+    // Many evictions (the first compression after a long prefill): every CTA sorts its 256
+    // keys (bitonic network in shared memory); after a cluster barrier each key counts the
+    // smaller keys of every CTA by binary search in that CTA's sorted list (DSMEM).
+    if (!skip) lst[tid] = mykey;
+    __syncthreads();
+    for (int k2 = 2; k2 <= kKeysPerCta; k2 <<= 1)
+      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+        if (!skip && tid < kKeysPerCta / 2) {
+          const int i = 2 * tid - (tid & (j2 - 1));
+          const unsigned long long x = lst[i], y = lst[i + j2];
+          if ((x > y) == ((i & k2) == 0)) {
+            lst[i] = y;
+            lst[i + j2] = x;
+          }
+        }
+        __syncthreads();
+      }
+    cluster_sync();  // every CTA's sorted list is complete
+    if (!skip && key_valid) {
+      int pos[kMaxCluster];
+      uint32_t base[kMaxCluster];
+#pragma unroll
+      for (int cc = 0; cc < kMaxCluster; ++cc) {
+        pos[cc] = 0;
+        base[cc] = mapa(smem_u32(lst), cc < C ? cc : 0);
+      }
+#pragma unroll
+      for (int step = kKeysPerCta / 2; step > 0; step >>= 1)
+#pragma unroll
+        for (int cc = 0; cc < kMaxCluster; ++cc)
+          if (cc < C && ld_cluster_u64(base[cc] + 8u * static_cast<uint32_t>(pos[cc] + step - 1)) < mykey)
+            pos[cc] += step;
+      int rank = 0;
+#pragma unroll
+      for (int cc = 0; cc < kMaxCluster; ++cc) rank += (cc < C) ? pos[cc] : 0;
+      evicted = rank < E;
+    }
+    const int kept_cta = __syncthreads_count(!skip && key_valid && !evicted);
+    if (!skip && tid == 0) {
+      const uint32_t local = smem_u32(&s.kept_recv[c]);
+      for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), static_cast<uint32_t>(kept_cta));
+    }
+  }
+  if (!skip && tid == 0) {
+    bool vok = true;
+    if (v_pending) {
+      vok = mbar_wait_bounded(&s.bar_v, ph_v, kWaitNs);  // staged V rows have landed
       if (vok) {
         ph_v ^= 1;
         v_pending = false;
       }
-      ok = ok && vok;
-      const uint32_t local = smem_u32(&s.status_recv[c]);
-      for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), (fail || !ok) ? 1u : 0u);
     }
+    ok = ok && vok;
+    const uint32_t local = smem_u32(&s.status_recv[c]);
+    for (int dst = 0; dst < C; ++dst) st_cluster_u32(mapa(local, dst), (fail || !ok) ? 1u : 0u);
   }
   if (c == 0 && tid == 0) {  // the next unit reaches every CTA with this barrier, skipped or not
     const uint32_t nl = smem_u32(&s.next_unit[iter & 1]);
@@ -574,43 +637,51 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool any_fail = false;
   if (!skip) {
     for (int cc = 0; cc < C; ++cc) any_fail |= s.status_recv[cc] != 0;
-    const int E = a.E;
-    // cluster level: merge the C sorted lists (missing lists count as +inf), identically in
-    // every CTA; the first E keys of the result are evicted
-    // scratch in u0: the u1 buffers may already receive the next unit's row statistics
-    unsigned long long* const m4 = s.u0.lists;       // [4][32]
-    unsigned long long* const m2 = s.u0.lists + 128; // [2][32]
-    if (warp < 4) {
-      const unsigned long long x0 = (2 * warp < C) ? s.cand_recv[(2 * warp) * 32 + lane] : ~0ull;
-      const unsigned long long x1 = (2 * warp + 1 < C) ? s.cand_recv[(2 * warp + 1) * 32 + lane] : ~0ull;
-      m4[warp * 32 + lane] = warp_merge_low32(x0, x1, lane);
-    }
-    __syncthreads();
-    if (warp < 2) m2[warp * 32 + lane] = warp_merge_low32(m4[(2 * warp) * 32 + lane], m4[(2 * warp + 1) * 32 + lane], lane);
-    __syncthreads();
-    if (warp == 0) {
-      const unsigned long long fin = warp_merge_low32(m2[lane], m2[32 + lane], lane);
-      if (lane < E) s.evict_pos[lane] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(fin & 0xFFFFFFFFu));
-    }
-    __syncthreads();
-
-    // destination of this CTA's keys: j = t - #(evicted before t); -1 = nothing to move
-    int j = -1;
-    bool evicted = false;
-    if (key_valid) {
-      int shift = 0;
-      for (int e = 0; e < E; ++e) {
-        const int p = s.evict_pos[e];
-        shift += (p < kt) ? 1 : 0;
-        evicted |= (p == kt);
+    int j = -1;  // destination slot of this thread's key if kept
+    if (E <= 32) {
+      // cluster level: merge the C sorted lists (missing lists count as +inf), identically in
+      // every CTA; the first E keys of the result are evicted.  Scratch in u0: the u1 buffers
+      // may already receive the next unit's row statistics.
+      unsigned long long* const m4 = s.u0.lists;        // [4][32]
+      unsigned long long* const m2 = s.u0.lists + 128;  // [2][32]
+      if (warp < 4) {
+        const unsigned long long x0 = (2 * warp < C) ? s.cand_recv[(2 * warp) * 32 + lane] : ~0ull;
+        const unsigned long long x1 = (2 * warp + 1 < C) ? s.cand_recv[(2 * warp + 1) * 32 + lane] : ~0ull;
+        m4[warp * 32 + lane] = warp_merge_low32(x0, x1, lane);
       }
-      if (!evicted) {
-        j = kt - shift;
-        g_in = a.decay * g_in + attn;  // global-score update of the kept key
+      __syncthreads();
+      if (warp < 2)
+        m2[warp * 32 + lane] = warp_merge_low32(m4[(2 * warp) * 32 + lane], m4[(2 * warp + 1) * 32 + lane], lane);
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned long long fin = warp_merge_low32(m2[lane], m2[32 + lane], lane);
+        if (lane < E) s.evict_pos[lane] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(fin & 0xFFFFFFFFu));
       }
-      if (a.dbg_keep)
-        a.dbg_keep[((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * L + kt] = evicted ? 0 : 1;
+      __syncthreads();
+      // j = t - #(evicted before t)
+      if (key_valid) {
+        int shift = 0;
+        for (int e = 0; e < E; ++e) {
+          const int p = s.evict_pos[e];
+          shift += (p < kt) ? 1 : 0;
+          evicted |= (p == kt);
+        }
+        if (!evicted) j = kt - shift;
+      }
+    } else {
+      // j = kept keys of the earlier CTAs + kept keys before t in this CTA
+      const bool kept = key_valid && !evicted;
+      const unsigned ball = __ballot_sync(0xffffffffu, kept);
+      if (lane == 0) s.warp_kept[warp] = __popc(ball);
+      __syncthreads();
+      int before = 0;
+      for (int cc = 0; cc < c; ++cc) before += s.kept_recv[cc];
+      for (int ww = 0; ww < warp; ++ww) before += s.warp_kept[ww];
+      if (kept) j = before + __popc(ball & ((1u << lane) - 1));
     }
+    if (j >= 0) g_in = a.decay * g_in + attn;  // global-score update of the kept key
+    if (key_valid && a.dbg_keep)
+      a.dbg_keep[((static_cast<int64_t>(r) * a.layers + layer) * a.Hkv + h) * La + kt] = j >= 0 ? 1 : 0;
     const bool moved = j >= 0 && (s.src_tab[kt >> bs] != s.dst_tab[j >> bs] || (kt & bm) != (j & bm));
     s.dst_of[tid] = moved ? j : -1;
     __syncthreads();
@@ -636,9 +707,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<uint4*>(dk + a.kv_bytes) = vv;
         }
       }
-      float* G = a.gscores + ((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * L;
+      float* G = a.gscores + ((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * La;
       if (j >= 0) G[j] = g_in;
-      if (c == C - 1 && tid < a.E) G[a.k + tid] = 0.0f;
+      if (kt >= a.k && kt < L) G[kt] = 0.0f;  // slots past the k survivors
     }
   }
   if (!skip && any_fail && tid == 0 && c == 0) record_error(a.err, ZP_ERR_TIMEOUT);
@@ -685,8 +756,11 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
             b = p->block_size, n_max = p->n_max, w = p->window, R = meta->num_requests;
   if (layers <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || R < 0 || num_qslots <= 0) return ZP_ERR_INVALID_ARG;
   if (n_max < 2 || meta->max_blocks < n_max || w < 1) return ZP_ERR_INVALID_ARG;
-  const int L = n_max * b, k = (n_max - 1) * b, Gq = Hq / Hkv, Rw = w * Gq;
-  if (w > k) return ZP_ERR_INVALID_ARG;
+  const int k = (n_max - 1) * b, Gq = Hq / Hkv, Rw = w * Gq;
+  // launch length: the longest request of the call (n_max*b unless the caller says more)
+  const int L = meta->max_seq_len > 0 ? meta->max_seq_len : n_max * b;
+  if (w > k || L <= k) return ZP_ERR_INVALID_ARG;
+  if (meta->max_blocks < (L + b - 1) / b) return ZP_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ZP_ERR_UNSUPPORTED;
   if (b != 16 && b != 32) return ZP_ERR_UNSUPPORTED;
   if (Rw > kRows || n_max > kMaxTable || (L + kKeysPerCta - 1) / kKeysPerCta > kMaxCluster)
@@ -741,7 +815,6 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.Rw = Rw;
   a.L = L;
   a.k = k;
-  a.E = L - k;
   a.max_blocks = meta->max_blocks;
   a.num_qslots = num_qslots;
   a.alpha = p->alpha;
@@ -749,7 +822,6 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.decay = p->decay;
   a.sl2 = p->scale * 1.4426950408889634f;
   a.inv_rw = 1.0f / static_cast<float>(Rw);
-  a.inv_bm1 = 1.0f / static_cast<float>(b - 1);
   a.row_bytes = static_cast<uint32_t>(d) * 2;
   a.b_shift = (b == 16) ? 4 : 5;
   a.kv_bytes = static_cast<uint32_t>(Hkv) * b * a.row_bytes;

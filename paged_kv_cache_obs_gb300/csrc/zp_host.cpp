@@ -272,16 +272,21 @@ zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, i
 }
 
 zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R,
-                             int32_t max_blocks, int32_t n_max, zp_stream stream) {
+                             int32_t max_blocks, int32_t n_max, int32_t block_size, const int32_t* host_seq_len,
+                             zp_stream stream) {
   if (!a || R < 0 || n_max < 2 || max_blocks < n_max || (R > 0 && (!old_tables || !new_tables)))
     return ZP_ERR_INVALID_ARG;
+  if (host_seq_len && block_size <= 0) return ZP_ERR_INVALID_ARG;
   std::vector<int32_t> release;
   for (int32_t r = 0; r < R; ++r) {
     const int32_t* o = old_tables + static_cast<int64_t>(r) * max_blocks;
     const int32_t* n = new_tables + static_cast<int64_t>(r) * max_blocks;
     for (int32_t i = 0; i < n_max - 1; ++i)
       if (o[i] != n[i]) release.push_back(o[i]);
-    release.push_back(o[n_max - 1]);
+    // every block past the first n_max - 1: one at the decode trigger, more after a prefill
+    const int32_t nblk = host_seq_len ? (host_seq_len[r] + block_size - 1) / block_size : n_max;
+    if (nblk < n_max || nblk > max_blocks) return ZP_ERR_INVALID_ARG;
+    for (int32_t i = n_max - 1; i < nblk; ++i) release.push_back(o[i]);
   }
   return zp_decref_after(a, release.data(), static_cast<int32_t>(release.size()), stream);
 }

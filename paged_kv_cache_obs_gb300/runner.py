@@ -39,9 +39,15 @@ class CompressionBatch:
         self.gs = inp.global_scores.to(dev)
         self.workspace = zipage.new_workspace(zipage.zp_compress_workspace_size(self.params, R), dev)
         self.debug = None
+        # the row length of the global scores is the longest sequence the call may hold (more
+        # than n_max*b only when requests left a long prefill)
+        self.seq_len = np.ascontiguousarray(inp.seq_len[:R])
+        row = inp.global_scores.shape[-1]
+        self.max_seq_len = row if row != wl.L else 0
 
     def enable_debug(self):
-        R, nl, Hkv, L = self.inp.num_compress, self.wl.num_layers, self.wl.num_kv_heads, self.wl.L
+        R, nl, Hkv = self.inp.num_compress, self.wl.num_layers, self.wl.num_kv_heads
+        L = self.max_seq_len or self.wl.L
         z = lambda dt: torch.zeros((R, nl, Hkv, L), dtype=dt, device=self.device)
         self.debug = {"attn": z(torch.float32), "redund": z(torch.float32), "score": z(torch.float32),
                       "keep": z(torch.int32)}
@@ -49,13 +55,15 @@ class CompressionBatch:
 
     def launch(self, stream=None):
         zipage.zp_compress(self.pool, self.d_tables, self.d_seq, self.d_qslot, self.d_dst, self.obs_q,
-                           self.gs, self.params, self.workspace, debug=self.debug, stream=stream)
+                           self.gs, self.params, self.workspace, debug=self.debug, stream=stream,
+                           max_seq_len=self.max_seq_len)
 
     def error(self, stream=None) -> int:
         return zipage.zp_read_error(self.workspace, stream)
 
     def commit(self, stream=None):
-        zipage.zp_commit_compress(self.alloc, self.tables, self.dst_tables, self.wl.n_max, stream=stream)
+        zipage.zp_commit_compress(self.alloc, self.tables, self.dst_tables, self.wl.n_max, stream=stream,
+                                  block_size=self.wl.block_size, seq_len=self.seq_len)
 
     def close(self):
         if self.alloc is not None:

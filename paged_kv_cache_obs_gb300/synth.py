@@ -17,6 +17,8 @@ Workloads (sizes as in the workload list of this project):
   mixed        llama3_8b shape, 256 running requests: 32 hold query slots at N_max = 128 full
                blocks and compress; 224 decode with U{1..128} blocks and a last-block fill of
                U{1..16} tokens
+  prefill      llama3_8b shape with N_max 64 (k = 1008): 64 requests that left a long prefill and
+               hold U{1009..2048} tokens each (first compression after the prompt); G ~ U(0,1)
 Physical block ids are a seeded random permutation over the pool in every workload.
 Seeds: 0x5A1F0000 + workload index.
 """
@@ -45,6 +47,7 @@ class Workload:
     global_init: str = "uniform"      # zeros | uniform
     shared_prefix_blocks: int = 0
     num_decode: int = 0               # mixed workload: requests that only decode
+    prefill_max: int = 0              # > n_max*b: compressing requests hold U{k+1..prefill_max} tokens
     pool_blocks: int = 0              # 0 = just enough (+ targets), else this many
     alpha: float = 0.5
     beta: float = 0.5
@@ -80,6 +83,8 @@ WORKLOADS = {
                               key_recipe="clustered", shared_prefix_blocks=16),
     "mixed": Workload("mixed", 4, 32, 32, 32, 8, 128, 16, 128, 32, key_recipe="clustered",
                       num_decode=224),
+    "prefill": Workload("prefill", 5, 64, 32, 32, 8, 128, 16, 64, 32, key_recipe="clustered",
+                        prefill_max=2048),
 }
 
 
@@ -136,6 +141,13 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
     # ---- logical -> physical block assignment ---------------------------------------
     counts = [n_max] * R
     fills = [b] * R
+    L_row = L  # row length of the global scores: the longest sequence
+    if wl.prefill_max > L:
+        k_keep = (n_max - 1) * b
+        lens = rng.integers(k_keep + 1, wl.prefill_max + 1, size=R)
+        counts = [int((x + b - 1) // b) for x in lens]
+        fills = [int(x - (c - 1) * b) for x, c in zip(lens, counts)]
+        L_row = wl.prefill_max
     if wl.num_decode:
         counts += list(rng.integers(1, n_max + 1, size=wl.num_decode))
         fills += list(rng.integers(1, b + 1, size=wl.num_decode))
@@ -145,7 +157,8 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
     NB = wl.pool_blocks or int(needed + targets + max(16, needed // 64))
     assert NB >= needed + targets
     perm = rng.permutation(NB).astype(np.int32)
-    tables = np.full((R_all, n_max), -1, dtype=np.int32)
+    max_blocks = max(n_max, max(counts), (L_row + b - 1) // b)
+    tables = np.full((R_all, max_blocks), -1, dtype=np.int32)
     nxt = 0
     shared = perm[nxt:nxt + P]
     nxt += P
@@ -193,13 +206,14 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
     M = R
     q = torch.randn((M, nl, w, Hq, d), generator=g, device=dev)
     if wl.key_recipe == "rope":
-        pos = (L - w + torch.arange(w, device=dev))[None, None, :, None].expand(M, nl, w, Hq)
+        last = torch.as_tensor(seq_len[:M], device=dev, dtype=torch.int64)
+        pos = (last[:, None] - w + torch.arange(w, device=dev)[None, :])[:, None, :, None].expand(M, nl, w, Hq)
         q = _rope_(q, pos, wl.rope_theta)
     obs_q = q.to(torch.bfloat16)
     if wl.global_init == "zeros":
-        gs = torch.zeros((M, nl, Hkv, L), dtype=torch.float32, device=dev)
+        gs = torch.zeros((M, nl, Hkv, L_row), dtype=torch.float32, device=dev)
     else:
-        gs = torch.rand((M, nl, Hkv, L), generator=g, device=dev, dtype=torch.float32)
+        gs = torch.rand((M, nl, Hkv, L_row), generator=g, device=dev, dtype=torch.float32)
 
     decode_q = None
     if wl.num_decode:

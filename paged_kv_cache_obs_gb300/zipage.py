@@ -54,7 +54,7 @@ class zp_kv_pool(ctypes.Structure):
 class zp_seq_meta(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("seq_len", ctypes.c_void_p), ("qslot", ctypes.c_void_p),
-                ("dst_tables", ctypes.c_void_p)]
+                ("dst_tables", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32)]
 
 
 class zp_debug(ctypes.Structure):
@@ -99,7 +99,7 @@ _sig("zp_refcount", _I32, [_P, _I32])
 _sig("zp_num_free", _I64, [_P])
 _sig("zp_num_pending", _I64, [_P])
 _sig("zp_plan_compress", _I32, [_P, _P, _I32, _I32, _I32, _P])
-_sig("zp_commit_compress", _I32, [_P, _P, _P, _I32, _I32, _I32, _P])
+_sig("zp_commit_compress", _I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P])
 _sig("zp_version", _I32, [])
 
 
@@ -138,11 +138,12 @@ def zp_compress_workspace_size(params: dict, num_requests: int) -> int:
 
 
 def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_scores, params: dict,
-                workspace, debug: dict | None = None, stream=None):
-    """Queues the compression pass; tensors are device tensors (see include/zipage.h)."""
+                workspace, debug: dict | None = None, stream=None, max_seq_len: int = 0):
+    """Queues the compression pass; tensors are device tensors (see include/zipage.h).
+    max_seq_len: the longest seq_len of the call (0: every request holds n_max*b tokens)."""
     kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
     meta = zp_seq_meta(block_tables.shape[0], block_tables.shape[1], seq_len.data_ptr(),
-                       qslot.data_ptr(), dst_tables.data_ptr())
+                       qslot.data_ptr(), dst_tables.data_ptr(), max_seq_len)
     dbg = None
     if debug:
         dbg = zp_debug(*(debug[k].data_ptr() if debug.get(k) is not None else None
@@ -268,14 +269,17 @@ def zp_plan_compress(a, host_tables, n_max: int):
     return out
 
 
-def zp_commit_compress(a, old_tables, new_tables, n_max: int, stream=None):
+def zp_commit_compress(a, old_tables, new_tables, n_max: int, stream=None, block_size: int = 0,
+                       seq_len=None):
+    """seq_len: host per-request token counts (None: every request holds n_max blocks)."""
     import numpy as np
     o = np.ascontiguousarray(old_tables, dtype=np.int32)
     n = np.ascontiguousarray(new_tables, dtype=np.int32)
+    sl = None if seq_len is None else np.ascontiguousarray(seq_len, dtype=np.int32)
     st = None if stream is False else _stream(stream)
-    _check("zp_commit_compress", lib.zp_commit_compress(a, o.ctypes.data_as(ctypes.c_void_p),
-                                                        n.ctypes.data_as(ctypes.c_void_p), o.shape[0],
-                                                        o.shape[1], n_max, st))
+    _check("zp_commit_compress", lib.zp_commit_compress(
+        a, o.ctypes.data_as(ctypes.c_void_p), n.ctypes.data_as(ctypes.c_void_p), o.shape[0], o.shape[1], n_max,
+        block_size, None if sl is None else sl.ctypes.data_as(ctypes.c_void_p), st))
 
 
 def zp_version() -> int:

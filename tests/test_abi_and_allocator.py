@@ -157,3 +157,25 @@ def test_invalid_arguments_are_rejected_without_a_gpu(zp):
     assert st == zp.ZP_ERR_INVALID_ARG
     assert zp.zp_compress_workspace_size(p, 4) >= 4
     assert zp.zp_paged_decode_workspace_size(dict(p, num_kv_heads=2), 3, 20) > 256
+
+
+def test_commit_after_prefill_releases_every_block_past_n_max_minus_1(zp):
+    a = zp.zp_alloc_create(64)
+    try:
+        n_max, b = 4, 16
+        ids = zp.zp_alloc_blocks(a, 7 + 4)          # request 0: 7 blocks, request 1: 4 blocks
+        tables = np.full((2, 8), -1, np.int32)
+        tables[0, :7] = ids[:7]
+        tables[1, :4] = ids[7:]
+        seq = np.array([7 * b - 5, 4 * b], np.int32)  # request 0 left a prefill of 107 tokens
+        dst = zp.zp_plan_compress(a, tables, n_max)
+        assert np.array_equal(dst, tables)            # nothing shared: in place
+        free0 = zp.zp_num_free(a)
+        zp.zp_commit_compress(a, tables, dst, n_max, stream=False, block_size=b, seq_len=seq)
+        assert zp.zp_num_free(a) == free0 + (7 - 3) + (4 - 3)
+        for i in list(ids[3:7]) + [ids[10]]:
+            assert zp.zp_refcount(a, int(i)) == 0
+        for i in list(ids[:3]) + list(ids[7:10]):
+            assert zp.zp_refcount(a, int(i)) == 1
+    finally:
+        zp.zp_alloc_destroy(a)

@@ -70,6 +70,14 @@ SMALL = {
     "no_protect_noncausal": synth.WORKLOADS["llama3_8b"].scaled(num_requests=1, num_layers=2, n_max=16,
                                                                 protect_window=0, causal=0),
     "one_window_row": synth.WORKLOADS["qwen2_7b"].scaled(num_requests=1, num_layers=1, n_max=8, window=1),
+    # first compression after a prefill: L in (k, 1100], k = 496, so E spans 1..604 (both
+    # selection paths), partial last blocks, and CTAs past a short request's end
+    "prefill_small": synth.WORKLOADS["prefill"].scaled(num_requests=4, num_layers=2, n_max=32, prefill_max=1100),
+    "prefill_d64_b32": synth.WORKLOADS["tiny"].scaled(num_requests=3, num_layers=2, num_q_heads=8, num_kv_heads=2,
+                                                      block_size=32, n_max=10, window=4, prefill_max=700,
+                                                      global_init="uniform"),
+    "prefill_one_cta": synth.WORKLOADS["prefill"].scaled(num_requests=3, num_layers=1, n_max=9, window=8,
+                                                         prefill_max=250),
 }
 
 
@@ -138,13 +146,15 @@ def test_unsupported_and_empty_calls(zp):
     batch.close()
 
 
-def test_wrong_seq_len_is_reported(zp):
+@pytest.mark.parametrize("bad_len", ["no_eviction", "too_long"])
+def test_wrong_seq_len_is_reported(zp, bad_len):
     zipage, runner = zp
     wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, n_max=8)
     inp = synth.make_inputs(wl, "cpu")
     pool_in = synth.bf16_bits(inp.pool)
     batch = runner.CompressionBatch(inp, "cuda")
-    batch.d_seq[0] = wl.L - 3
+    # a request must hold more than k = (n_max-1)*b tokens and at most the launch length
+    batch.d_seq[0] = (wl.n_max - 1) * wl.block_size if bad_len == "no_eviction" else wl.L + 1
     batch.launch()
     assert batch.error() == zipage.ZP_ERR_BAD_TABLE
     out = synth.bf16_bits(batch.pool)
@@ -155,25 +165,27 @@ def test_wrong_seq_len_is_reported(zp):
 
 # ------------------------------------------------------------------ full-size workloads -----
 
-FULL = ["qwen2_7b", "llama3_8b", "shared_prefix"]
+FULL = ["qwen2_7b", "llama3_8b", "shared_prefix", "prefill"]
 
 
 def _compaction_property_all_units(batch, pristine, keep):
     """Every unit: compacted row j equals input row src_j (bit-exact), k kept per head,
     protected window kept; blocks outside the destination tables are unchanged."""
     wl = batch.wl
-    b, k, L, w = wl.block_size, (wl.n_max - 1) * wl.block_size, wl.L, wl.window
+    b, k, w = wl.block_size, (wl.n_max - 1) * wl.block_size, wl.window
     nl, Hkv = wl.num_layers, wl.num_kv_heads
     counts = keep.sum(-1)
     assert bool((counts == k).all())
-    if wl.protect_window:
-        assert bool((keep[..., L - w:] == 1).all())
     dev = batch.pool.device
-    pos = torch.arange(L, device=dev)
     li = torch.arange(nl, device=dev)[:, None, None]
     hi = torch.arange(Hkv, device=dev)[None, :, None]
     for r in range(batch.inp.num_compress):
-        src = pos.expand(nl, Hkv, L)[keep[r].bool()].view(nl, Hkv, k)
+        L = int(batch.seq_len[r])
+        if wl.protect_window:
+            assert bool((keep[r, ..., L - w:L] == 1).all())
+        assert bool((keep[r, ..., L:] == 0).all())
+        pos = torch.arange(L, device=dev)
+        src = pos.expand(nl, Hkv, L)[keep[r, ..., :L].bool()].view(nl, Hkv, k)
         tab = torch.from_numpy(batch.tables[r]).to(dev).long()
         dtab = torch.from_numpy(batch.dst_tables[r]).to(dev).long()
         j = torch.arange(k, device=dev)
@@ -182,6 +194,7 @@ def _compaction_property_all_units(batch, pristine, keep):
             new = batch.pool[li, dtab[j // b][None, None, :], kv, hi, (j % b)[None, None, :]]
             assert torch.equal(old.view(torch.int16), new.view(torch.int16)), f"request {r} kv {kv}"
     written = set(batch.dst_tables[:, :wl.n_max - 1].ravel().tolist())
+    written.discard(-1)
     others = torch.tensor(sorted(set(range(batch.pool.shape[1])) - written), device=dev)
     assert torch.equal(pristine[:, others].view(torch.int16), batch.pool[:, others].view(torch.int16))
 
@@ -209,10 +222,11 @@ def test_full_size_sampled_units_and_properties(zp, name):
     # oracle inputs restricted to the sampled requests (their blocks only)
     sub_tables = batch.tables[reqs]
     sub_dst = batch.dst_tables[reqs]
-    blocks = sorted(set(sub_tables[:, :wl.n_max].ravel().tolist()) | set(sub_dst[:, :wl.n_max].ravel().tolist()))
+    blocks = sorted((set(sub_tables.ravel().tolist()) | set(sub_dst.ravel().tolist())) - {-1})
     remap = {blk: i for i, blk in enumerate(blocks)}
-    rt = np.vectorize(remap.get)(sub_tables[:, :wl.n_max]).astype(np.int32)
-    rd = np.vectorize(remap.get)(sub_dst[:, :wl.n_max]).astype(np.int32)
+    remap[-1] = -1
+    rt = np.vectorize(remap.get)(sub_tables).astype(np.int32)
+    rd = np.vectorize(remap.get)(sub_dst).astype(np.int32)
     bidx = torch.tensor(blocks, device="cuda")
     pool_in = synth.bf16_bits(pristine[:, bidx])
     pool_out = synth.bf16_bits(batch.pool[:, bidx])

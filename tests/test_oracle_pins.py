@@ -327,3 +327,30 @@ def test_bf16_round_trip():
     assert back[1] == 1.0 and back[2] == -2.5 and back[3] == 3.140625
     # round to nearest even at the halfway point 1 + 2^-8
     assert O.bf16_bits_to_f64(O.f64_to_bf16_bits(np.array([1 + 2 ** -8])))[0] == 1.0
+
+
+def test_pass_invariants_after_prefill():
+    # requests longer than n_max*b (first compression after a long prompt): still exactly k
+    # kept per head, the freed slots of the global score zeroed up to the request's length
+    from paged_kv_cache_obs_gb300 import synth
+    wl = synth.WORKLOADS["prefill"].scaled(num_requests=3, num_layers=1, num_kv_heads=2, num_q_heads=4,
+                                            n_max=6, window=8, prefill_max=300)
+    inp = synth.make_inputs(wl, "cpu")
+    pool = synth.bf16_bits(inp.pool)
+    obs_q = synth.bf16_bits(inp.obs_q)
+    gs = inp.global_scores.numpy()
+    R = inp.num_compress
+    t = inp.block_tables[:R]
+    new_pool, new_G, dbg = O.compress_pass(pool, t, t, inp.seq_len[:R], inp.qslot, obs_q, gs, wl.params())
+    b = wl.block_size
+    k = (wl.n_max - 1) * b
+    assert (inp.seq_len[:R] > k).all() and (inp.seq_len[:R] <= 300).all()
+    for (r, l, h), u in dbg.items():
+        L = int(inp.seq_len[r])
+        assert len(u["attn"]) == L and len(u["src"]) == k
+        assert set(range(L - wl.window, L)) <= set(u["src"].tolist())
+        assert (new_G[r, l, h, k:L] == 0).all()
+        assert np.array_equal(new_G[r, l, h, L:], gs[r, l, h, L:])   # beyond L untouched
+        k_in = O.gather_rows(pool, l, 0, h, t[r], L, b)
+        k_out = O.gather_rows(new_pool, l, 0, h, t[r], k, b)
+        assert np.array_equal(k_out, k_in[u["src"]])
