@@ -87,6 +87,10 @@ typedef struct zp_seq_meta {
   int32_t max_seq_len;        /* L_max: the longest seq_len of the call (<= 2048), or 0 for
                                  n_max*b.  It is also the row length of global_scores and of
                                  the zp_debug arrays. */
+  const int32_t* n_max_per_req; /* device [R] or NULL: per-request block budgets
+                                   2 <= N_max_r <= params.n_max (the pages' per-request dynamic
+                                   budgets, de §5); request r keeps k_r = (N_max_r-1)*b tokens per
+                                   head.  NULL: every request uses params.n_max. */
 } zp_seq_meta;
 
 /* Optional per-token outputs, each device [R][num_layers][num_kv_heads][L_max] (row-major),
@@ -224,6 +228,9 @@ int64_t zp_num_pending(const zp_alloc* a);           /* blocks waiting in deferr
  * Transactional: ZP_ERR_NO_BLOCKS leaves the allocator unchanged. */
 zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks,
                            int32_t n_max, int32_t* host_dst_tables);
+/* As zp_plan_compress with a per-request budget host_n_max[R] (2 <= N_max_r <= max_blocks). */
+zp_status zp_plan_compress_budgets(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks,
+                                   const int32_t* host_n_max, int32_t* host_dst_tables);
 
 /* After the compression launched on `stream`: for each request, decref every replaced shared
  * block (old != new for i < n_max-1) and every old block past the first n_max-1
@@ -233,6 +240,10 @@ zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, i
 zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables,
                              int32_t R, int32_t max_blocks, int32_t n_max, int32_t block_size,
                              const int32_t* host_seq_len, zp_stream stream);
+/* As zp_commit_compress with a per-request budget host_n_max[R] (NULL: n_max for all). */
+zp_status zp_commit_compress_budgets(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables,
+                                     int32_t R, int32_t max_blocks, const int32_t* host_n_max, int32_t n_max,
+                                     int32_t block_size, const int32_t* host_seq_len, zp_stream stream);
 
 /* Library version, for the binding's sanity check. */
 int32_t zp_version(void);

@@ -73,7 +73,7 @@ def expected_pool(pool_in, tables, dst_tables, srcs, b):
 
 
 def check_units(units, pool_in, obs_q, gs_in, tables, dst_tables, seq_len, qslot, params,
-                dbg_gpu, gs_out, pool_out=None, full_pool=False):
+                dbg_gpu, gs_out, pool_out=None, full_pool=False, n_max_per_req=None):
     """Checks the given units against the oracle.
 
     dbg_gpu: dict of numpy arrays attn/redund/score/keep shaped [R, layers, Hkv, L].
@@ -82,16 +82,16 @@ def check_units(units, pool_in, obs_q, gs_in, tables, dst_tables, seq_len, qslot
     compared with the expected pool (requires units to cover every unit).
     Returns the number of tokens whose selection differs from the fp64 oracle.
     """
-    b, n_max = params["block_size"], params["n_max"]
-    k = (n_max - 1) * b
+    b = params["block_size"]
     _, _, ref = O.compress_pass(pool_in, tables, dst_tables, seq_len, qslot, obs_q, gs_in, params,
-                                units=units)
+                                units=units, n_max_per_req=n_max_per_req)
     srcs = {}
     ndiff = 0
     for (r, l, h) in units:
         u = ref[(r, l, h)]
         where = f" at unit (r={r}, layer={l}, h={h})"
         L = int(seq_len[r])
+        k = ((int(n_max_per_req[r]) if n_max_per_req is not None else params["n_max"]) - 1) * b
         assert_close("attn", dbg_gpu["attn"][r, l, h][:L], u["attn"], where)
         assert_close("redundancy", dbg_gpu["redund"][r, l, h][:L], u["R"], where)
         assert_close("score", dbg_gpu["score"][r, l, h][:L], u["S"], where)

@@ -218,7 +218,7 @@ def score_unit(q_bits, k_bits, G, *, b, n_max, window, alpha, beta, scale, prote
 
 
 def compress_pass(pool, block_tables, dst_tables, seq_len, qslot, obs_q, global_scores, p,
-                  units=None):
+                  units=None, n_max_per_req=None):
     """The compression pass over every (request, layer, kv head) unit, on copies of the state.
 
     pool          uint16 [layers, num_blocks, 2, Hkv, b, d]   (index 0 = K, 1 = V)
@@ -231,6 +231,8 @@ def compress_pass(pool, block_tables, dst_tables, seq_len, qslot, obs_q, global_
     p             dict with num_q_heads, num_kv_heads, block_size, n_max, window, alpha, beta,
                   decay, scale, protect_window, causal
     units         optional iterable of (r, layer, h) to compute; default all.
+    n_max_per_req optional per-request block budgets (default p["n_max"] for every request);
+                  request r keeps k_r = (N_max_r - 1) * b tokens per head.
 
     Returns (new_pool, new_global_scores, debug) where debug maps (r, layer, h) to a dict with
     attn, R, S (float64 [L]) and src (int64 [k]).  Units are independent: every read of the
@@ -239,8 +241,7 @@ def compress_pass(pool, block_tables, dst_tables, seq_len, qslot, obs_q, global_
     layers, _, _, Hkv, b, d = pool.shape
     Hq = p["num_q_heads"]
     Gq = Hq // Hkv
-    n_max, w = p["n_max"], p["window"]
-    k_keep = (n_max - 1) * b
+    w = p["window"]
     new_pool = pool.copy()
     new_G = np.array(global_scores, dtype=np.float32, copy=True)
     debug = {}
@@ -249,6 +250,8 @@ def compress_pass(pool, block_tables, dst_tables, seq_len, qslot, obs_q, global_
         units = [(r, l, h) for r in range(R_req) for l in range(layers) for h in range(Hkv)]
     for (r, l, h) in units:
         L = int(seq_len[r])
+        n_max = int(n_max_per_req[r]) if n_max_per_req is not None else p["n_max"]
+        k_keep = (n_max - 1) * b
         table, dtab = block_tables[r], dst_tables[r]
         rows = [slot_location(table, t, b) for t in range(L)]
         k_bits = np.stack([pool[l, blk, 0, h, row] for blk, row in rows])

@@ -53,6 +53,7 @@ struct CompressArgs {
   const int32_t* dst_tables;
   const int32_t* seq_len;
   const int32_t* qslot;
+  const int32_t* n_max_req;         // per-request block budgets, or nullptr
   float* gscores;
   int32_t* err;
   int32_t* work;                    // unit counter of the persistent clusters (zeroed per launch)
@@ -250,20 +251,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   // all take the same decision without communicating.  A request holds L cached tokens with
   // k < L <= La (L = n_max*b at the decode trigger; more after a long prefill).
   const int L = a.seq_len[r];
-  bool bad = (L <= a.k) || (L > La) || slot < 0 || slot >= a.num_qslots;
+  // the request's block budget (all requests share n_max unless per-request budgets are given)
+  const int n_max_r = a.n_max_req ? a.n_max_req[r] : a.n_max;
+  const int k_r = (n_max_r - 1) * b;                 // tokens this request keeps per head
+  bool bad = (n_max_r < 2) || (n_max_r > a.n_max) || (k_r < w) || (L <= k_r) || (L > La) || slot < 0 ||
+             slot >= a.num_qslots;
   const int nblk_req = bad ? 0 : (L + bm) >> bs;
   for (int i = tid; i < nblk_req; i += kThreads) {
     const int sb = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + i];
     s.src_tab[i] = sb;
     bad |= (sb < 0 || sb >= a.num_blocks);
   }
-  for (int i = tid; i < a.n_max - 1; i += kThreads) {
+  for (int i = tid; i < (bad ? 0 : n_max_r - 1); i += kThreads) {
     const int db = a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + i];
     s.dst_tab[i] = db;
     bad |= (db < 0 || db >= a.num_blocks);
   }
   const int nk = max(0, min(kKeysPerCta, L - t0));   // this unit's keys in this CTA
-  const int E = L - a.k;                              // tokens to evict per head
+  const int E = L - k_r;                              // tokens to evict per head
   // Zero the padding rows of Q (never touched by the TMA box; the V staging of the previous
   // unit may have used them).
   for (int i = Rw * 8 + tid; i < kRows * 8; i += kThreads) {
@@ -709,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       float* G = a.gscores + ((static_cast<int64_t>(slot) * a.layers + layer) * a.Hkv + h) * La;
       if (j >= 0) G[j] = g_in;
-      if (kt >= a.k && kt < L) G[kt] = 0.0f;  // slots past the k survivors
+      if (kt >= k_r && kt < L) G[kt] = 0.0f;  // slots past the k survivors
     }
   }
   if (!skip && any_fail && tid == 0 && c == 0) record_error(a.err, ZP_ERR_TIMEOUT);
@@ -794,6 +799,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.dst_tables = meta->dst_tables;
   a.seq_len = meta->seq_len;
   a.qslot = meta->qslot;
+  a.n_max_req = meta->n_max_per_req;
   a.gscores = global_scores;
   a.err = static_cast<int32_t*>(workspace);
   a.work = static_cast<int32_t*>(workspace) + 1;

@@ -240,17 +240,21 @@ zp_status zp_alloc_inject_failure(zp_alloc* a, int64_t nth_call) {
   return ZP_OK;
 }
 
-zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks,
-                           int32_t n_max, int32_t* host_dst_tables) {
-  if (!a || R < 0 || n_max < 2 || max_blocks < n_max || (R > 0 && (!host_tables || !host_dst_tables)))
-    return ZP_ERR_INVALID_ARG;
+namespace {
+// Plan with a budget per request (host_n_max) or one budget for all (n_max_all).
+zp_status plan_impl(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks, const int32_t* host_n_max,
+                    int32_t n_max_all, int32_t* host_dst_tables) {
+  if (!a || R < 0 || (R > 0 && (!host_tables || !host_dst_tables))) return ZP_ERR_INVALID_ARG;
+  auto nmax_of = [&](int32_t r) { return host_n_max ? host_n_max[r] : n_max_all; };
+  for (int32_t r = 0; r < R; ++r)
+    if (nmax_of(r) < 2 || nmax_of(r) > max_blocks) return ZP_ERR_INVALID_ARG;
   poll_pending(a, false);
   int64_t need = 0;
   for (int32_t r = 0; r < R; ++r)
-    for (int32_t i = 0; i < n_max; ++i) {
+    for (int32_t i = 0; i < nmax_of(r); ++i) {
       const int32_t id = host_tables[static_cast<int64_t>(r) * max_blocks + i];
       if (!valid_id(a, id) || a->refcount[id] <= 0) return ZP_ERR_INVALID_ARG;
-      if (i < n_max - 1 && a->refcount[id] > 1) ++need;
+      if (i < nmax_of(r) - 1 && a->refcount[id] > 1) ++need;
     }
   std::vector<int32_t> fresh(static_cast<size_t>(need));
   if (need > 0) {
@@ -262,23 +266,24 @@ zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, i
     for (int32_t i = 0; i < max_blocks; ++i) {
       const int64_t o = static_cast<int64_t>(r) * max_blocks + i;
       const int32_t id = host_tables[o];
-      if (i >= n_max - 1) {
+      if (i >= nmax_of(r) - 1) {
         host_dst_tables[o] = id;
         continue;
       }
-      host_dst_tables[o] = (i < n_max - 1 && a->refcount[id] > 1) ? fresh[next++] : id;
+      host_dst_tables[o] = (a->refcount[id] > 1) ? fresh[next++] : id;
     }
   return ZP_OK;
 }
 
-zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R,
-                             int32_t max_blocks, int32_t n_max, int32_t block_size, const int32_t* host_seq_len,
-                             zp_stream stream) {
-  if (!a || R < 0 || n_max < 2 || max_blocks < n_max || (R > 0 && (!old_tables || !new_tables)))
-    return ZP_ERR_INVALID_ARG;
+zp_status commit_impl(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R, int32_t max_blocks,
+                      const int32_t* host_n_max, int32_t n_max_all, int32_t block_size, const int32_t* host_seq_len,
+                      zp_stream stream) {
+  if (!a || R < 0 || (R > 0 && (!old_tables || !new_tables))) return ZP_ERR_INVALID_ARG;
   if (host_seq_len && block_size <= 0) return ZP_ERR_INVALID_ARG;
   std::vector<int32_t> release;
   for (int32_t r = 0; r < R; ++r) {
+    const int32_t n_max = host_n_max ? host_n_max[r] : n_max_all;
+    if (n_max < 2 || n_max > max_blocks) return ZP_ERR_INVALID_ARG;
     const int32_t* o = old_tables + static_cast<int64_t>(r) * max_blocks;
     const int32_t* n = new_tables + static_cast<int64_t>(r) * max_blocks;
     for (int32_t i = 0; i < n_max - 1; ++i)
@@ -289,6 +294,32 @@ zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32
     for (int32_t i = n_max - 1; i < nblk; ++i) release.push_back(o[i]);
   }
   return zp_decref_after(a, release.data(), static_cast<int32_t>(release.size()), stream);
+}
+}  // namespace
+
+zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks, int32_t n_max,
+                           int32_t* host_dst_tables) {
+  if (n_max < 2 || max_blocks < n_max) return ZP_ERR_INVALID_ARG;
+  return plan_impl(a, host_tables, R, max_blocks, nullptr, n_max, host_dst_tables);
+}
+
+zp_status zp_plan_compress_budgets(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks,
+                                   const int32_t* host_n_max, int32_t* host_dst_tables) {
+  if (!host_n_max && R > 0) return ZP_ERR_INVALID_ARG;
+  return plan_impl(a, host_tables, R, max_blocks, host_n_max, 0, host_dst_tables);
+}
+
+zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R,
+                             int32_t max_blocks, int32_t n_max, int32_t block_size, const int32_t* host_seq_len,
+                             zp_stream stream) {
+  if (n_max < 2 || max_blocks < n_max) return ZP_ERR_INVALID_ARG;
+  return commit_impl(a, old_tables, new_tables, R, max_blocks, nullptr, n_max, block_size, host_seq_len, stream);
+}
+
+zp_status zp_commit_compress_budgets(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R,
+                                     int32_t max_blocks, const int32_t* host_n_max, int32_t n_max, int32_t block_size,
+                                     const int32_t* host_seq_len, zp_stream stream) {
+  return commit_impl(a, old_tables, new_tables, R, max_blocks, host_n_max, n_max, block_size, host_seq_len, stream);
 }
 
 zp_status zp_read_error(void* workspace, zp_stream stream, zp_status* out_status) {

@@ -27,7 +27,11 @@ class CompressionBatch:
         if len(extra):
             zipage.zp_incref(self.alloc, extra)
         self.tables = np.ascontiguousarray(inp.block_tables[:R])
-        self.dst_tables = zipage.zp_plan_compress(self.alloc, self.tables, wl.n_max)
+        self.n_max_req = inp.n_max_req
+        if self.n_max_req is None:
+            self.dst_tables = zipage.zp_plan_compress(self.alloc, self.tables, wl.n_max)
+        else:
+            self.dst_tables = zipage.zp_plan_compress_budgets(self.alloc, self.tables, self.n_max_req)
         dev = torch.device(device)
         self.device = dev
         self.pool = pool if pool is not None else inp.pool.to(dev)
@@ -38,6 +42,7 @@ class CompressionBatch:
         self.obs_q = inp.obs_q.to(dev)
         self.gs = inp.global_scores.to(dev)
         self.workspace = zipage.new_workspace(zipage.zp_compress_workspace_size(self.params, R), dev)
+        self.d_nmax = None if self.n_max_req is None else torch.from_numpy(self.n_max_req).to(dev)
         self.debug = None
         # the row length of the global scores is the longest sequence the call may hold (more
         # than n_max*b only when requests left a long prefill)
@@ -56,14 +61,19 @@ class CompressionBatch:
     def launch(self, stream=None):
         zipage.zp_compress(self.pool, self.d_tables, self.d_seq, self.d_qslot, self.d_dst, self.obs_q,
                            self.gs, self.params, self.workspace, debug=self.debug, stream=stream,
-                           max_seq_len=self.max_seq_len)
+                           max_seq_len=self.max_seq_len, n_max_per_req=self.d_nmax)
 
     def error(self, stream=None) -> int:
         return zipage.zp_read_error(self.workspace, stream)
 
     def commit(self, stream=None):
-        zipage.zp_commit_compress(self.alloc, self.tables, self.dst_tables, self.wl.n_max, stream=stream,
-                                  block_size=self.wl.block_size, seq_len=self.seq_len)
+        if self.n_max_req is None:
+            zipage.zp_commit_compress(self.alloc, self.tables, self.dst_tables, self.wl.n_max, stream=stream,
+                                      block_size=self.wl.block_size, seq_len=self.seq_len)
+        else:
+            zipage.zp_commit_compress_budgets(self.alloc, self.tables, self.dst_tables, self.n_max_req,
+                                              self.wl.n_max, stream=stream, block_size=self.wl.block_size,
+                                              seq_len=self.seq_len)
 
     def close(self):
         if self.alloc is not None:

@@ -48,6 +48,8 @@ class Workload:
     shared_prefix_blocks: int = 0
     num_decode: int = 0               # mixed workload: requests that only decode
     prefill_max: int = 0              # > n_max*b: compressing requests hold U{k+1..prefill_max} tokens
+    budget_min: int = 0               # > 0: per-request budgets N_max_r ~ U{budget_min..n_max}, each
+                                      # request at its own trigger (N_max_r full blocks)
     pool_blocks: int = 0              # 0 = just enough (+ targets), else this many
     alpha: float = 0.5
     beta: float = 0.5
@@ -123,6 +125,7 @@ class Inputs:
     refcount: np.ndarray           # int32 [NB] refcount of every physical block
     num_compress: int
     decode_q: torch.Tensor | None  # bf16 [layers, num_decode, Hq, d] (mixed workload)
+    n_max_req: np.ndarray | None = None  # int32 [R] per-request budgets (or None)
 
 
 def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
@@ -148,6 +151,10 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
         counts = [int((x + b - 1) // b) for x in lens]
         fills = [int(x - (c - 1) * b) for x, c in zip(lens, counts)]
         L_row = wl.prefill_max
+    n_max_req = None
+    if wl.budget_min:
+        n_max_req = rng.integers(wl.budget_min, n_max + 1, size=R).astype(np.int32)
+        counts = [int(x) for x in n_max_req]
     if wl.num_decode:
         counts += list(rng.integers(1, n_max + 1, size=wl.num_decode))
         fills += list(rng.integers(1, b + 1, size=wl.num_decode))
@@ -221,7 +228,7 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
 
     return Inputs(wl=wl, pool=pool, block_tables=tables, seq_len=seq_len,
                   qslot=np.arange(R, dtype=np.int32), obs_q=obs_q, global_scores=gs,
-                  refcount=refcount, num_compress=R, decode_q=decode_q)
+                  refcount=refcount, num_compress=R, decode_q=decode_q, n_max_req=n_max_req)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

@@ -54,7 +54,8 @@ class zp_kv_pool(ctypes.Structure):
 class zp_seq_meta(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("seq_len", ctypes.c_void_p), ("qslot", ctypes.c_void_p),
-                ("dst_tables", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32)]
+                ("dst_tables", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
+                ("n_max_per_req", ctypes.c_void_p)]
 
 
 class zp_debug(ctypes.Structure):
@@ -100,6 +101,8 @@ _sig("zp_num_free", _I64, [_P])
 _sig("zp_num_pending", _I64, [_P])
 _sig("zp_plan_compress", _I32, [_P, _P, _I32, _I32, _I32, _P])
 _sig("zp_commit_compress", _I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P])
+_sig("zp_plan_compress_budgets", _I32, [_P, _P, _I32, _I32, _P, _P])
+_sig("zp_commit_compress_budgets", _I32, [_P, _P, _P, _I32, _I32, _P, _I32, _I32, _P, _P])
 _sig("zp_version", _I32, [])
 
 
@@ -138,12 +141,14 @@ def zp_compress_workspace_size(params: dict, num_requests: int) -> int:
 
 
 def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_scores, params: dict,
-                workspace, debug: dict | None = None, stream=None, max_seq_len: int = 0):
+                workspace, debug: dict | None = None, stream=None, max_seq_len: int = 0, n_max_per_req=None):
     """Queues the compression pass; tensors are device tensors (see include/zipage.h).
-    max_seq_len: the longest seq_len of the call (0: every request holds n_max*b tokens)."""
+    max_seq_len: the longest seq_len of the call (0: every request holds n_max*b tokens).
+    n_max_per_req: optional device int32 [R] of per-request block budgets."""
     kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
     meta = zp_seq_meta(block_tables.shape[0], block_tables.shape[1], seq_len.data_ptr(),
-                       qslot.data_ptr(), dst_tables.data_ptr(), max_seq_len)
+                       qslot.data_ptr(), dst_tables.data_ptr(), max_seq_len,
+                       None if n_max_per_req is None else n_max_per_req.data_ptr())
     dbg = None
     if debug:
         dbg = zp_debug(*(debug[k].data_ptr() if debug.get(k) is not None else None
@@ -267,6 +272,31 @@ def zp_plan_compress(a, host_tables, n_max: int):
                                                     t.shape[1], n_max,
                                                     out.ctypes.data_as(ctypes.c_void_p)))
     return out
+
+
+def zp_plan_compress_budgets(a, host_tables, n_max_per_req):
+    import numpy as np
+    t = np.ascontiguousarray(host_tables, dtype=np.int32)
+    nm = np.ascontiguousarray(n_max_per_req, dtype=np.int32)
+    out = np.zeros_like(t)
+    _check("zp_plan_compress_budgets", lib.zp_plan_compress_budgets(
+        a, t.ctypes.data_as(ctypes.c_void_p), t.shape[0], t.shape[1], nm.ctypes.data_as(ctypes.c_void_p),
+        out.ctypes.data_as(ctypes.c_void_p)))
+    return out
+
+
+def zp_commit_compress_budgets(a, old_tables, new_tables, n_max_per_req, n_max: int, stream=None,
+                               block_size: int = 0, seq_len=None):
+    import numpy as np
+    o = np.ascontiguousarray(old_tables, dtype=np.int32)
+    n = np.ascontiguousarray(new_tables, dtype=np.int32)
+    nm = np.ascontiguousarray(n_max_per_req, dtype=np.int32)
+    sl = None if seq_len is None else np.ascontiguousarray(seq_len, dtype=np.int32)
+    st = None if stream is False else _stream(stream)
+    _check("zp_commit_compress_budgets", lib.zp_commit_compress_budgets(
+        a, o.ctypes.data_as(ctypes.c_void_p), n.ctypes.data_as(ctypes.c_void_p), o.shape[0], o.shape[1],
+        nm.ctypes.data_as(ctypes.c_void_p), n_max, block_size,
+        None if sl is None else sl.ctypes.data_as(ctypes.c_void_p), st))
 
 
 def zp_commit_compress(a, old_tables, new_tables, n_max: int, stream=None, block_size: int = 0,

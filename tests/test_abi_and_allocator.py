@@ -179,3 +179,27 @@ def test_commit_after_prefill_releases_every_block_past_n_max_minus_1(zp):
             assert zp.zp_refcount(a, int(i)) == 1
     finally:
         zp.zp_alloc_destroy(a)
+
+
+def test_plan_and_commit_with_per_request_budgets(zp):
+    a = zp.zp_alloc_create(40)
+    try:
+        # request 0: budget 3 with a shared first block; request 1: budget 5, nothing shared
+        ids = zp.zp_alloc_blocks(a, 3 + 5)
+        tables = np.full((2, 6), -1, np.int32)
+        tables[0, :3] = ids[:3]
+        tables[1, :5] = ids[3:8]
+        zp.zp_incref(a, [ids[0]])                          # block ids[0] is shared
+        dst = zp.zp_plan_compress_budgets(a, tables, [3, 5])
+        assert dst[0, 0] != tables[0, 0] and zp.zp_refcount(a, int(dst[0, 0])) == 1   # target block
+        assert np.array_equal(dst[0, 1:], tables[0, 1:]) and np.array_equal(dst[1], tables[1])
+        free0 = zp.zp_num_free(a)
+        zp.zp_commit_compress_budgets(a, tables, dst, [3, 5], 5, stream=False)
+        # released: the replaced shared block (decref only), the last block of each request
+        assert zp.zp_refcount(a, int(ids[0])) == 1
+        assert zp.zp_refcount(a, int(ids[2])) == 0 and zp.zp_refcount(a, int(ids[7])) == 0
+        assert zp.zp_num_free(a) == free0 + 2
+        with pytest.raises(zp.ZipageError):
+            zp.zp_plan_compress_budgets(a, tables, [1, 5])  # a budget below 2
+    finally:
+        zp.zp_alloc_destroy(a)

@@ -49,7 +49,8 @@ def _check_all(zp, wl, **kw):
     dbg = {k: v.cpu().numpy() for k, v in batch.debug.items()}
     ndiff = parity.check_units(units, pool_in, obs_q, gs_in, batch.tables, batch.dst_tables,
                                inp.seq_len[:R], inp.qslot, wl.params(), dbg,
-                               batch.gs.cpu().numpy(), synth.bf16_bits(batch.pool), full_pool=True)
+                               batch.gs.cpu().numpy(), synth.bf16_bits(batch.pool), full_pool=True,
+                               n_max_per_req=inp.n_max_req)
     batch.close()
     return ndiff
 
@@ -78,6 +79,10 @@ SMALL = {
                                                       global_init="uniform"),
     "prefill_one_cta": synth.WORKLOADS["prefill"].scaled(num_requests=3, num_layers=1, n_max=9, window=8,
                                                          prefill_max=250),
+    # per-request budgets N_max_r in 3..40, each request at its own trigger (N_max_r full blocks):
+    # clusters of 1..3 active CTAs under a launch of 3
+    "budgets_small": synth.WORKLOADS["llama3_8b"].scaled(num_requests=5, num_layers=2, n_max=40, window=16,
+                                                         budget_min=3),
 }
 
 

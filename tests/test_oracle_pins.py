@@ -354,3 +354,22 @@ def test_pass_invariants_after_prefill():
         k_in = O.gather_rows(pool, l, 0, h, t[r], L, b)
         k_out = O.gather_rows(new_pool, l, 0, h, t[r], k, b)
         assert np.array_equal(k_out, k_in[u["src"]])
+
+
+def test_per_request_budgets_keep_their_own_k():
+    # request r keeps (N_max_r - 1) * b tokens per head (per-request budgets)
+    from paged_kv_cache_obs_gb300 import synth
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=4, num_layers=1, num_kv_heads=2, num_q_heads=4,
+                                              n_max=10, window=8, budget_min=2)
+    inp = synth.make_inputs(wl, "cpu")
+    R = inp.num_compress
+    t = inp.block_tables[:R]
+    _, new_G, dbg = O.compress_pass(synth.bf16_bits(inp.pool), t, t, inp.seq_len[:R], inp.qslot,
+                                    synth.bf16_bits(inp.obs_q), inp.global_scores.numpy(), wl.params(),
+                                    n_max_per_req=inp.n_max_req)
+    b = wl.block_size
+    for (r, l, h), u in dbg.items():
+        k_r = (int(inp.n_max_req[r]) - 1) * b
+        assert int(inp.seq_len[r]) == int(inp.n_max_req[r]) * b
+        assert len(u["src"]) == k_r
+        assert (new_G[r, l, h, k_r:int(inp.seq_len[r])] == 0).all()
