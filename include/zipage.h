@@ -245,6 +245,67 @@ zp_status zp_commit_compress_budgets(zp_alloc* a, const int32_t* old_tables, con
                                      int32_t R, int32_t max_blocks, const int32_t* host_n_max, int32_t n_max,
                                      int32_t block_size, const int32_t* host_seq_len, zp_stream stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Hybrid scheduler (zh §2.2, de §2 "Hybrid Scheduling", es §2, fr §2.B).  Host only.
+ *
+ * Plans engine steps around the compression pass: only the first num_slots running requests
+ * (admission order) hold a query slot; requests below n_max blocks, or whose last block still
+ * has room, decode without one; a request at n_max blocks with a full last block (or longer,
+ * after a prefill) compresses if it holds a slot and waits otherwise; when a block cannot be
+ * allocated the most recently admitted request without a slot is preempted (it returns to the
+ * front of the queue and recomputes); with none left the step runs in restricted mode (only
+ * slot holders grow).  Blocks come from the given allocator; compressions keep the first
+ * n_max-1 blocks and release the rest when the next step applies them.
+ * --------------------------------------------------------------------------------------- */
+typedef struct zp_sched zp_sched;
+
+typedef struct zp_sched_config {
+  int32_t n_max;        /* block cap per request */
+  int32_t block_size;   /* b */
+  int32_t num_slots;    /* M query slots */
+  int32_t max_running;  /* cap on running requests, 0 = none */
+} zp_sched_config;
+
+/* The plan of one step; the arrays belong to the scheduler and stay valid until the next
+ * zp_sched_step or zp_sched_destroy. */
+typedef struct zp_sched_plan {
+  int32_t num_decode;           /* requests that decode one token */
+  const int32_t* decode_ids;
+  int32_t num_compress;         /* requests whose compression runs this step (async) */
+  const int32_t* compress_ids;
+  int32_t num_prefill;          /* requests admitted this step */
+  const int32_t* prefill_ids;
+  int32_t num_preempted;        /* requests preempted this step */
+  const int32_t* preempted_ids;
+  int32_t restricted;           /* 1: this step ran in restricted mode */
+} zp_sched_plan;
+
+typedef struct zp_sched_request_info {
+  int32_t state;                /* 0 waiting, 1 running, 2 finished */
+  int32_t seq_len;              /* cached tokens */
+  int32_t generated;            /* tokens decoded so far */
+  int32_t num_blocks;
+  const int32_t* table;         /* host [num_blocks], valid until the next step */
+  int32_t has_slot;
+  int32_t preemptions;
+} zp_sched_request_info;
+
+typedef struct zp_sched_stats {
+  int64_t steps, submitted, admitted, finished, decoded_tokens, compressions, preemptions, slot_waits,
+      restricted_steps, blocks_in_use;
+  int32_t running;
+} zp_sched_stats;
+
+zp_status zp_sched_create(zp_alloc* alloc, const zp_sched_config* cfg, zp_sched** out);
+void zp_sched_destroy(zp_sched* s);
+/* Queues a request of prompt_len tokens that will decode gen_len tokens; *req_id = its id. */
+zp_status zp_sched_submit(zp_sched* s, int32_t prompt_len, int32_t gen_len, int32_t* req_id);
+/* Applies the previous step's plan (decoded tokens, compressions, finished requests) and
+ * plans the next one. */
+zp_status zp_sched_step(zp_sched* s, zp_sched_plan* plan);
+zp_status zp_sched_request(const zp_sched* s, int32_t req_id, zp_sched_request_info* info);
+zp_status zp_sched_get_stats(const zp_sched* s, zp_sched_stats* out);
+
 /* Library version, for the binding's sanity check. */
 int32_t zp_version(void);
 

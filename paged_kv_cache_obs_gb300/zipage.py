@@ -106,6 +106,37 @@ _sig("zp_commit_compress_budgets", _I32, [_P, _P, _P, _I32, _I32, _P, _I32, _I32
 _sig("zp_version", _I32, [])
 
 
+class zp_sched_config(ctypes.Structure):
+    _fields_ = [("n_max", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+                ("max_running", ctypes.c_int32)]
+
+
+class zp_sched_plan(ctypes.Structure):
+    _fields_ = [("num_decode", ctypes.c_int32), ("decode_ids", _I32P), ("num_compress", ctypes.c_int32),
+                ("compress_ids", _I32P), ("num_prefill", ctypes.c_int32), ("prefill_ids", _I32P),
+                ("num_preempted", ctypes.c_int32), ("preempted_ids", _I32P), ("restricted", ctypes.c_int32)]
+
+
+class zp_sched_request_info(ctypes.Structure):
+    _fields_ = [("state", ctypes.c_int32), ("seq_len", ctypes.c_int32), ("generated", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("table", _I32P), ("has_slot", ctypes.c_int32),
+                ("preemptions", ctypes.c_int32)]
+
+
+class zp_sched_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("steps", "submitted", "admitted", "finished", "decoded_tokens",
+                                               "compressions", "preemptions", "slot_waits", "restricted_steps",
+                                               "blocks_in_use")] + [("running", ctypes.c_int32)]
+
+
+_sig("zp_sched_create", _I32, [_P, ctypes.POINTER(zp_sched_config), ctypes.POINTER(_P)])
+_sig("zp_sched_destroy", None, [_P])
+_sig("zp_sched_submit", _I32, [_P, _I32, _I32, _I32P])
+_sig("zp_sched_step", _I32, [_P, ctypes.POINTER(zp_sched_plan)])
+_sig("zp_sched_request", _I32, [_P, _I32, ctypes.POINTER(zp_sched_request_info)])
+_sig("zp_sched_get_stats", _I32, [_P, ctypes.POINTER(zp_sched_stats)])
+
+
 def _check(fn, status):
     if status != ZP_OK:
         raise ZipageError(fn, status)
@@ -314,3 +345,45 @@ def zp_commit_compress(a, old_tables, new_tables, n_max: int, stream=None, block
 
 def zp_version() -> int:
     return lib.zp_version()
+
+
+# ------------------------------------------------------------------ hybrid scheduler (host) --
+
+def zp_sched_create(alloc, n_max: int, block_size: int, num_slots: int, max_running: int = 0):
+    h = ctypes.c_void_p()
+    cfg = zp_sched_config(n_max, block_size, num_slots, max_running)
+    _check("zp_sched_create", lib.zp_sched_create(alloc, ctypes.byref(cfg), ctypes.byref(h)))
+    return h
+
+
+def zp_sched_destroy(s):
+    lib.zp_sched_destroy(s)
+
+
+def zp_sched_submit(s, prompt_len: int, gen_len: int) -> int:
+    rid = ctypes.c_int32()
+    _check("zp_sched_submit", lib.zp_sched_submit(s, prompt_len, gen_len, ctypes.byref(rid)))
+    return rid.value
+
+
+def zp_sched_step(s) -> dict:
+    p = zp_sched_plan()
+    _check("zp_sched_step", lib.zp_sched_step(s, ctypes.byref(p)))
+    ids = lambda n, ptr: [ptr[i] for i in range(n)]
+    return {"decode": ids(p.num_decode, p.decode_ids), "compress": ids(p.num_compress, p.compress_ids),
+            "prefill": ids(p.num_prefill, p.prefill_ids), "preempted": ids(p.num_preempted, p.preempted_ids),
+            "restricted": bool(p.restricted)}
+
+
+def zp_sched_request(s, rid: int) -> dict:
+    i = zp_sched_request_info()
+    _check("zp_sched_request", lib.zp_sched_request(s, rid, ctypes.byref(i)))
+    return {"state": i.state, "seq_len": i.seq_len, "generated": i.generated, "num_blocks": i.num_blocks,
+            "table": [i.table[k] for k in range(i.num_blocks)], "has_slot": bool(i.has_slot),
+            "preemptions": i.preemptions}
+
+
+def zp_sched_get_stats(s) -> dict:
+    st = zp_sched_stats()
+    _check("zp_sched_get_stats", lib.zp_sched_get_stats(s, ctypes.byref(st)))
+    return {n: getattr(st, n) for n, _ in zp_sched_stats._fields_}
