@@ -76,7 +76,6 @@ struct __align__(1024) Smem {
   uint8_t Q[2][kRows * 128];
   union {
     float2 part[2][kRows];          // pass-1 (max, sum) per column half
-    float norm[kKeysPerCta];        // reciprocal key norms (Gram diagonal)
     unsigned long long lists[192];  // cluster-level merge of the eviction candidates
   } u0;
   union {
@@ -93,6 +92,7 @@ struct __align__(1024) Smem {
   int src_tab[kMaxTable];
   int dst_tab[kMaxTable];
   int dst_of[kKeysPerCta];          // destination slot of each key that moves, else -1
+  float inv_n[kKeysPerCta];         // reciprocal key norms (Gram diagonal)
   uint64_t bar_tma;
   uint64_t bar_mma;
   uint64_t bar_v;
@@ -164,6 +164,82 @@ __device__ __forceinline__ void record_error(int32_t* err, int code) {
 __device__ __forceinline__ size_t row_off_bytes(const CompressArgs& a, int phys, int kv, int row) {
   return static_cast<size_t>(static_cast<uint32_t>(phys)) * a.block_bytes + kv * a.kv_bytes +
          static_cast<uint32_t>(row) * a.row_bytes;
+}
+
+// Lightning redundancy of the 32 keys [key0, key0 + 32) of one warp (BW = block size 16 or 32),
+// from K in 128-byte-swizzled shared memory, with warp-level mma.sync: the BW x BW Gram of each
+// block (G = K K^T, so one ldmatrix per k-step gives both the A and the B fragments), squared
+// norms from its diagonal, and the in-block row sums of cos(k_t, k_j), j != t, over the tokens
+// the block holds (keys at or past L are excluded).  Returns the redundancy of key key0 + lane.
+template <int BW>
+__device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2][kKeysPerCta * 128], float* inv_n,
+                                                           int key0, int lane, int d, int t0, int L) {
+  constexpr int NT = BW / 8;  // n8 tiles per m16 row tile
+  float acc[2][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
+  for (int ks = 0; ks < (d >> 4); ++ks) {
+    uint32_t f[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int row = key0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int chunk = 2 * ks + (lane >> 4);
+      ldmatrix_x4(smem_u32(&K[chunk >> 3][row * 128 + (((chunk & 7) ^ (row & 7)) << 4)]), f[mt]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        // columns 8nt..8nt+7 of the block: rows (sub = nt&1) of m-tile src of the same fragments
+        const int src = (BW == 16) ? mt : (nt >> 1);
+        const int sub = nt & 1;
+        mma_16816_bf16(acc[mt][nt], f[mt], sub ? f[src][1] : f[src][0], sub ? f[src][3] : f[src][2]);
+      }
+  }
+  const int g = lane >> 2, tq = lane & 3;
+  // squared norms from the diagonal -> reciprocal norms in shared memory
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = 16 * mt + g + 8 * (e >> 1);
+        const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + (e & 1);
+        if (row == col) inv_n[key0 + row] = 1.0f / fmaxf(sqrtf(fmaxf(acc[mt][nt][e], 0.0f)), 1e-12f);
+      }
+  __syncwarp();
+  float rr[2][2];  // redundancy of rows 16mt + 8hf + g
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int row = 16 * mt + 8 * hf + g;
+      float sum = 0.0f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + e;
+          const bool ok = col != row && t0 + key0 + col < L;
+          sum += ok ? acc[mt][nt][2 * hf + e] * inv_n[key0 + col] : 0.0f;
+        }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      const int bstart = (BW == 16) ? 16 * mt : 0;             // block of this row within the warp
+      const int m = min(BW, L - (t0 + key0 + bstart));         // tokens the block holds
+      rr[mt][hf] = m > 1 ? sum * inv_n[key0 + row] / static_cast<float>(m - 1) : 0.0f;
+    }
+  // deliver: lane k takes row k, computed by lane 4 * (k % 8)
+  const int srcl = 4 * (lane & 7);
+  const float v00 = __shfl_sync(0xffffffffu, rr[0][0], srcl), v01 = __shfl_sync(0xffffffffu, rr[0][1], srcl);
+  const float v10 = __shfl_sync(0xffffffffu, rr[1][0], srcl), v11 = __shfl_sync(0xffffffffu, rr[1][1], srcl);
+  const int mt = lane >> 4, hf = (lane >> 3) & 1;
+  return mt ? (hf ? v11 : v10) : (hf ? v01 : v00);
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -380,15 +456,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
 
-  // ---- step 3: Gram of each 128-key half into TMEM (D1 fully read) while the row partials
-  //      go to every CTA of the cluster.
+  // ---- step 3: D2 = K Q^T per 128-key half into TMEM (D1 fully read) while the row partials
+  //      go to every CTA of the cluster.  The cluster barrier is split: the Lightning
+  //      redundancy (warp-level MMA on K in shared memory) is computed while the others arrive.
   if (!skip) {
     if (tid == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
       for (int kh = 0; kh < 2 && kh * 128 < nk_l; ++kh)
         for (int kk = 0; kk < d / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32]));
-          mma_bf16(tbase + kh * 128, ad, ad, idesc, kk > 0);
+          const uint64_t bd = smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32]));
+          mma_bf16(tbase + kh * 128, ad, bd, idesc, kk > 0);
         }
       mma_commit(&s.bar_mma);
     }
@@ -404,7 +482,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int dst = 0; dst < C; ++dst) st_cluster_v2(mapa(local, dst), m, l);
     }
   }
-  cluster_sync();  // #1: every CTA's row partials have landed
+  __syncwarp();
+  cluster_arrive();  // #1: this CTA's row partials are out
+  const int wcol = hh * 128 + q4 * 32;  // first key of this warp (TMEM lanes of pass 2)
+  if (!skip && warp * 32 < nk) {
+    red = (b == 16) ? warp_lightning_redundancy<16>(s.K, s.inv_n, warp * 32, lane, d, t0, L)
+                    : warp_lightning_redundancy<32>(s.K, s.inv_n, warp * 32, lane, d, t0, L);
+  }
+  cluster_wait();    // #1: every CTA's row partials have landed
 
   if (!skip) {
     if (tid < kRows) {
@@ -417,63 +502,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (p.y > 0.0f) Lsum += p.y * ex2((p.x - M) * a.sl2);
         }
       s.row_off[tid] = (tid < Rw && Lsum > 0.0f) ? fmaf(M, a.sl2, lg2(Lsum)) : INFINITY;
-    }
-    if (tid == 0) {
-      ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
-      ph_mma ^= 1;
-    }
-  }
-  fail |= __syncthreads_or(!ok);
-  tc_fence_after();
-
-  // ---- step 4: Lightning redundancy from the Gram (thread = key)
-  float gv[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) gv[j] = 0.0f;
-  const int wcol = hh * 128 + q4 * 32;  // first key (and Gram column) of this warp
-  float inv_nt = 0.0f;
-  if (!skip) {
-    if (wcol < nk) tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + wcol, gv);
-    float diag = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j == lane) diag = gv[j];
-    inv_nt = 1.0f / fmaxf(sqrtf(fmaxf(diag, 0.0f)), 1e-12f);
-    s.u0.norm[tid] = inv_nt;  // reciprocal key norms
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (!skip) {
-    // D2 = K Q^T per 128-key half into the same TMEM columns (Gram fully read)
-    if (tid == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, 128);
-      for (int kh = 0; kh < 2 && kh * 128 < nk_l; ++kh)
-        for (int kk = 0; kk < d / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32]));
-          const uint64_t bd = smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32]));
-          mma_bf16(tbase + kh * 128, ad, bd, idesc, kk > 0);
-        }
-      mma_commit(&s.bar_mma);
-    }
-    if (key_valid) {
-      const int jb0 = (tid & 31) & ~bm;  // first column of this key's block within gv
-      const int jlim = min(jb0 + b, L - t0 - (tid & ~31));  // columns of the block that hold tokens
-      const int m = jlim - jb0;                             // tokens in this key's block
-      const float4* inv4 = reinterpret_cast<const float4*>(&s.u0.norm[tid & ~31]);
-      float acc0 = 0.0f, acc1 = 0.0f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 nv = inv4[q];
-        const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * q + e;
-          const float cv = (j >= jb0 && j < jlim && j != lane) ? gv[j] * nn[e] : 0.0f;
-          if (e & 1) acc1 += cv; else acc0 += cv;
-        }
-      }
-      red = m > 1 ? (acc0 + acc1) * inv_nt / static_cast<float>(m - 1) : 0.0f;
     }
     if (tid == 0) {
       ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
