@@ -96,11 +96,16 @@ struct __align__(1024) Smem {
   uint64_t bar_tma;
   uint64_t bar_mma;
   uint64_t bar_v;
+  uint64_t bar_rs;                  // row statistics of every CTA of the cluster have landed
   uint32_t tmem_base;
   int next_unit[2];                 // unit after the current one, pushed by cluster rank 0
   int kept_recv[kMaxCluster];       // kept keys of every CTA (many-eviction path)
   int warp_kept[kThreads / 32];
 };
+
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA, plus the
+// 1 KB alignment slack of the dynamic allocation
+static_assert(sizeof(Smem) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "shared memory must allow two CTAs per SM");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -270,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&s.bar_tma, 1);
     mbar_init(&s.bar_mma, 1);
     mbar_init(&s.bar_v, 1);
+    mbar_init(&s.bar_rs, 1);
     fence_mbar_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmQ);
@@ -283,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   // mbarrier phases, tracked by the waiting thread (tid 0): every unit completes bar_tma once,
   // bar_v once (unless skipped) and bar_mma three times (unless skipped)
   uint32_t ph_tma = 0, ph_mma = 0, ph_v = 0;
+  // bar_rs completes once per unit that is not skipped; every thread tracks its phase (skip is
+  // uniform across the cluster)
+  uint32_t ph_rs = 0;
 
   // Persistent clusters: cluster i starts with unit i and then takes the next unused unit from
   // a global counter (fetched by cluster rank 0, broadcast through shared memory); a unit is
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* const head_base = a.pool + static_cast<size_t>(layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
                              static_cast<size_t>(h) * b * a.row_bytes;
 
-  // ---- set-up of the unit.  Thread 0 issues the TMA of K and Q straight away from the table
+  // ---- set-up of the unit.  Warp 0 issues the TMA of K and Q straight away from the table
   //      entries it reads itself; a block id outside the pool only makes TMA fill zeros, and
   //      the unit is then skipped after validation below (waiting for the copies).
   const int slot = a.qslot[r];
@@ -329,19 +338,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int L = a.seq_len[r];
   // the request's block budget (all requests share n_max unless per-request budgets are given)
   const int n_max_r = a.n_max_req ? a.n_max_req[r] : a.n_max;
+  // Every table entry the launch may use is loaded now, independently of L and of the budget,
+  // so that these loads overlap the two above; only the request's own entries are checked.
+  const int nblk_a = (La + bm) >> bs;  // <= kMaxTable <= kThreads
+  const int sb = tid < nblk_a ? a.block_tables[static_cast<int64_t>(r) * a.max_blocks + tid] : 0;
+  const int db = tid < a.n_max - 1 ? a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + tid] : 0;
   const int k_r = (n_max_r - 1) * b;                 // tokens this request keeps per head
   bool bad = (n_max_r < 2) || (n_max_r > a.n_max) || (k_r < w) || (L <= k_r) || (L > La) || slot < 0 ||
              slot >= a.num_qslots;
-  const int nblk_req = bad ? 0 : (L + bm) >> bs;
-  for (int i = tid; i < nblk_req; i += kThreads) {
-    const int sb = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + i];
-    s.src_tab[i] = sb;
-    bad |= (sb < 0 || sb >= a.num_blocks);
+  if (tid < nblk_a) {
+    s.src_tab[tid] = sb;
+    if (tid < ((L + bm) >> bs)) bad |= (sb < 0 || sb >= a.num_blocks);
   }
-  for (int i = tid; i < (bad ? 0 : n_max_r - 1); i += kThreads) {
-    const int db = a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + i];
-    s.dst_tab[i] = db;
-    bad |= (db < 0 || db >= a.num_blocks);
+  if (tid < a.n_max - 1) {
+    s.dst_tab[tid] = db;
+    if (tid < n_max_r - 1) bad |= (db < 0 || db >= a.num_blocks);
   }
   const int nk = max(0, min(kKeysPerCta, L - t0));   // this unit's keys in this CTA
   const int E = L - k_r;                              // tokens to evict per head
@@ -357,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool skip = __syncthreads_or(bad);
   tc_fence_after();
   if (skip && tid == 0 && c == 0) record_error(a.err, ZP_ERR_BAD_TABLE);
+  // every CTA of the cluster (this one included) delivers 128 row partials of 8 bytes here
+  if (!skip && tid == 0) mbar_arrive_expect_tx(&s.bar_rs, static_cast<uint32_t>(C * kRows * 8));
 
   const int kt = t0 + tid;  // the key this thread owns from pass 2 on
   const bool key_valid = tid < nk;
@@ -457,8 +470,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
 
   // ---- step 3: D2 = K Q^T per 128-key half into TMEM (D1 fully read) while the row partials
-  //      go to every CTA of the cluster.  The cluster barrier is split: the Lightning
-  //      redundancy (warp-level MMA on K in shared memory) is computed while the others arrive.
+  //      go to every CTA of the cluster as asynchronous stores that count on its bar_rs (no
+  //      cluster barrier).  The Lightning redundancy (warp-level MMA on K in shared memory) is
+  //      computed while they travel.
   if (!skip) {
     if (tid == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
@@ -478,21 +492,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (p0.y > 0.0f) l += p0.y * ex2((p0.x - m) * a.sl2);
         if (p1.y > 0.0f) l += p1.y * ex2((p1.x - m) * a.sl2);
       }
-      const uint32_t local = smem_u32(&s.u1.recv[c][tid]);
-      for (int dst = 0; dst < C; ++dst) st_cluster_v2(mapa(local, dst), m, l);
+      const uint32_t local = smem_u32(&s.u1.recv[c][tid]), lbar = smem_u32(&s.bar_rs);
+      for (int dst = 0; dst < C; ++dst) st_async_v2(mapa(local, dst), m, l, mapa(lbar, dst));
     }
   }
-  __syncwarp();
-  cluster_arrive();  // #1: this CTA's row partials are out
   const int wcol = hh * 128 + q4 * 32;  // first key of this warp (TMEM lanes of pass 2)
   if (!skip && warp * 32 < nk) {
     red = (b == 16) ? warp_lightning_redundancy<16>(s.K, s.inv_n, warp * 32, lane, d, t0, L)
                     : warp_lightning_redundancy<32>(s.K, s.inv_n, warp * 32, lane, d, t0, L);
   }
-  cluster_wait();    // #1: every CTA's row partials have landed
 
   if (!skip) {
     if (tid < kRows) {
+      // every CTA's row partials have landed (each combining thread waits for itself)
+      ok = mbar_wait_bounded_cluster(&s.bar_rs, ph_rs, kWaitNs) && ok;
       float M = -INFINITY;
       for (int cc = 0; cc < C; ++cc) M = fmaxf(M, s.u1.recv[cc][tid].x);
       float Lsum = 0.0f;
@@ -503,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       s.row_off[tid] = (tid < Rw && Lsum > 0.0f) ? fmaf(M, a.sl2, lg2(Lsum)) : INFINITY;
     }
+    ph_rs ^= 1;
     if (tid == 0) {
       ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs) && ok;
       ph_mma ^= 1;

@@ -47,6 +47,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// As mbar_try_wait, with acquire semantics at cluster scope: the data other CTAs of the cluster
+// delivered with st_async_v2 is visible to the caller once the phase has completed.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Waits for phase `parity` of the barrier to complete, for at most `limit_ns` nanoseconds.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
@@ -82,6 +106,13 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
           smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Hint: bring `bytes` (a multiple of 16) of global memory starting at `gsrc` (16-byte aligned)
+// into L2.  No completion is tracked.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -249,6 +280,14 @@ __device__ __forceinline__ uint32_t mapa(uint32_t local_addr, uint32_t rank) {
 
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// Non-blocking store of two floats to shared memory of a CTA of the cluster (`addr` from mapa);
+// its arrival counts 8 transaction bytes on the mbarrier at `bar_addr` (mapa) of that CTA.
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(bar_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
