@@ -403,14 +403,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
 
   // ---- step 2 (pass 1): per-row max and exp-sum over this CTA's keys.  Thread = window row
-  //      (TMEM lane), warp half hh = 128 key columns; two 32-column loads per wait; chunks that
-  //      every row sees completely take the unpredicated path.
+  //      (TMEM lane), warp half hh = 128 key columns; two 32-column loads per wait.  A group of
+  //      32 columns that every row sees completely takes the unpredicated path; the others
+  //      compare the column with this row's visibility limit (one compare per element).
   if (!skip) {
     const int i = q4 * 32 + lane;
-    const int t_lim = a.causal ? (L - w + i / Gq) : (L - 1);
-    const int vis_all = a.causal ? (L - w) : (L - 1);  // keys every window row sees
     const int cbase = hh * 128;
     const int ncol = nk - cbase;                         // valid columns of this half (may be <= 0)
+    // columns [0, vlim) of this half are visible to this row, [0, vall) to every row
+    const int vlim = max(0, min(ncol, (a.causal ? (L - w + i / Gq) : (L - 1)) - t0 - cbase + 1));
+    const int vall = max(0, min(ncol, (a.causal ? (L - w) : (L - 1)) - t0 - cbase + 1));
     const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     for (int c2 = 0; c2 < 2; ++c2) {
@@ -421,19 +423,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld32_issue(tl + col0 + 32, rb);
       tmem_wait_ld(ra);
       tmem_ld_dep(rb);
-      if (col0 + 64 <= ncol && t0 + cbase + col0 + 63 <= vis_all) {
+      if (col0 + 32 <= vall) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
-          mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
-        }
+        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
       } else {
+        const int lim = vlim - col0;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int cc = col0 + j;
-          const float v = __uint_as_float(j < 32 ? ra[j & 31] : rb[j & 31]);
-          if (cc < ncol && t0 + cbase + cc <= t_lim) mx[j & 3] = fmaxf(mx[j & 3], v);
-        }
+        for (int j = 0; j < 32; ++j)
+          if (j < lim) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+      }
+      if (col0 + 64 <= vall) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
+      } else {
+        const int lim = vlim - col0 - 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < lim) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
       }
     }
     const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -447,19 +453,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld32_issue(tl + col0 + 32, rb);
       tmem_wait_ld(ra);
       tmem_ld_dep(rb);
-      if (col0 + 64 <= ncol && t0 + cbase + col0 + 63 <= vis_all) {
+      if (col0 + 32 <= vall) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
-          ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
-        }
+        for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
       } else {
+        const int lim = vlim - col0;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int cc = col0 + j;
-          const float v = __uint_as_float(j < 32 ? ra[j & 31] : rb[j & 31]);
-          if (cc < ncol && t0 + cbase + cc <= t_lim) ls[j & 3] += ex2(fmaf(v, a.sl2, -mo));
-        }
+        for (int j = 0; j < 32; ++j)
+          if (j < lim) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
+      }
+      if (col0 + 64 <= vall) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
+      } else {
+        const int lim = vlim - col0 - 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < lim) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
       }
     }
     // rows without a visible key keep m = -inf and l = 0; padding rows are dropped below
