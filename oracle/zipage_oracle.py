@@ -122,6 +122,22 @@ def lightning_redundancy(k: np.ndarray, b: int) -> np.ndarray:
     return R
 
 
+def all_pairs_redundancy(k: np.ndarray) -> np.ndarray:
+    """The original redundancy that Lightning replaces (zh 2.1, es 2: O(N^2 b^2) pairs over the
+    N blocks of b tokens; de 2: it needs the full similarity matrix): R[t] = mean over every
+    other token j of the sequence of cos(k_t, k_j).  Same cosine and clamp as the Lightning
+    form; a sequence of one token has redundancy 0.  The full L x L cosine matrix is formed,
+    as that method does."""
+    L = k.shape[0]
+    R = np.zeros(L, dtype=np.float64)
+    if L < 2:
+        return R
+    norms = np.maximum(np.sqrt((k * k).sum(axis=1)), 1e-12)
+    unit = k / norms[:, None]
+    cos = unit @ unit.T  # L x L
+    return (cos.sum(axis=1) - np.diag(cos)) / (L - 1)
+
+
 # ----------------------------------------------------------------------------------------
 # Step 3 — combined importance score (zh 2.1 "评分机制": attention + redundancy + global).
 # ----------------------------------------------------------------------------------------

@@ -157,6 +157,51 @@ def test_redundancy_special_cases():
     np.testing.assert_allclose(O.lightning_redundancy(np.ones((3, 4)), 2), [1, 1, 0], atol=1e-14)
 
 
+def test_all_pairs_redundancy_closed_form():
+    """Sum over j != t of cos(k_t, k_j) is unit_t . (sum_j unit_j) - 1, so the all-pairs mean
+    needs no matrix: an independent formula for the same quantity."""
+    rng = np.random.default_rng(11)
+    for L in (2, 5, 64, 257):
+        k = rng.standard_normal((L, 24)) * rng.uniform(0.05, 8, size=(L, 1))
+        unit = k / np.linalg.norm(k, axis=1, keepdims=True)
+        want = (unit @ unit.sum(axis=0) - 1.0) / (L - 1)
+        np.testing.assert_allclose(O.all_pairs_redundancy(k), want, rtol=1e-11, atol=1e-13)
+
+
+def test_all_pairs_redundancy_special_cases():
+    rng = np.random.default_rng(12)
+    d = 16
+    # one block: all pairs are the block's pairs, so it is the Lightning score
+    k = rng.standard_normal((16, d))
+    np.testing.assert_allclose(O.all_pairs_redundancy(k), O.lightning_redundancy(k, 16), atol=1e-14)
+    # identical directions -> 1; orthonormal keys -> 0; a key and its negative -> -1
+    same = np.tile(rng.standard_normal(d), (9, 1)) * rng.uniform(0.5, 2, size=(9, 1))
+    np.testing.assert_allclose(O.all_pairs_redundancy(same), np.ones(9), atol=1e-14)
+    np.testing.assert_allclose(O.all_pairs_redundancy(np.eye(d)[:7] * 2.5), np.zeros(7), atol=1e-15)
+    v = rng.standard_normal(d)
+    np.testing.assert_allclose(O.all_pairs_redundancy(np.stack([v, -3 * v])), [-1, -1], atol=1e-14)
+    # a lone token has redundancy 0, and a zero key has cosine 0 with everything
+    np.testing.assert_allclose(O.all_pairs_redundancy(v[None, :]), [0.0])
+    z = np.stack([v, np.zeros(d), 2 * v])
+    np.testing.assert_allclose(O.all_pairs_redundancy(z), [0.5, 0.0, 0.5], atol=1e-14)
+
+
+def test_all_pairs_redundancy_brute_force():
+    """Pure-Python double loop over the pairs on a small input."""
+    rng = np.random.default_rng(13)
+    k = rng.standard_normal((11, 5))
+    L = k.shape[0]
+    want = []
+    for t in range(L):
+        acc = 0.0
+        for j in range(L):
+            if j != t:
+                dot = sum(float(k[t, e] * k[j, e]) for e in range(5))
+                acc += dot / (math.sqrt(sum(float(x * x) for x in k[t])) * math.sqrt(sum(float(x * x) for x in k[j])))
+        want.append(acc / (L - 1))
+    np.testing.assert_allclose(O.all_pairs_redundancy(k), want, rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------- selection ---------------
 
 def _brute_force_keep(S, k):
