@@ -500,6 +500,67 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_ablation(args):
+    """The Lightning ablation: the original all-pairs redundancy kernel alone against the whole
+    fused compression pass (whose redundancy is the Lightning form) on the same units, one GPU.
+    Defaults to 4 requests of the workload (the all-pairs kernel is O(L^2 d) per head)."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_obs_gb300 import runner, synth, zipage
+
+    torch.cuda.set_device(0)
+    if not args.requests:
+        args.requests = 4
+    wl = workload_of(args)
+    inp = synth.make_inputs(wl, "cuda")
+    pristine_pool = inp.pool.clone()
+    pristine_gs = inp.global_scores.clone()
+    batch = runner.CompressionBatch(inp, "cuda", pool=inp.pool)
+    stream = torch.cuda.Stream()
+    p = wl.params()
+    R = inp.num_compress
+    L = batch.max_seq_len or wl.L
+    redund = torch.empty((R, wl.num_layers, wl.num_kv_heads, L), device="cuda")
+    ws = zipage.new_workspace(zipage.zp_redundancy_workspace_size())
+
+    def timed(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                batch.pool.copy_(pristine_pool)
+                batch.gs.copy_(pristine_gs)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts))
+
+    ms_pass = timed(lambda: batch.launch(stream=stream))
+    assert batch.error(stream) == 0
+    ms_ap = timed(lambda: zipage.zp_redundancy_all_pairs(batch.pool, batch.d_tables, batch.d_seq, redund, p, ws,
+                                                         stream=stream, max_seq_len=batch.max_seq_len))
+    assert zipage.zp_read_error(ws, stream) == 0
+    units = R * wl.num_layers * wl.num_kv_heads
+    seq = np.asarray(inp.seq_len[:R], np.float64)
+    flops = float((2.0 * seq * seq * wl.head_dim).sum()) * wl.num_layers * wl.num_kv_heads
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak, tkind = float(json.load(f)["bf16_tflops"]), "measured (bf16_tflops burst)"
+    except (OSError, KeyError, ValueError):
+        tpeak, tkind = 1900.0, "fallback"
+    out = {"metric": "all-pairs redundancy vs the fused Lightning pass", "ablation": "lightning_vs_all_pairs",
+           "unit": "ms", "steps": args.steps, "warmup": args.warmup, "data": "synthetic (seeded)",
+           "config": {"workload": f"{wl.name}: {R} requests x {wl.num_layers} layers, {units} head units, L {L}"},
+           "fused_pass_ms": ms_pass, "all_pairs_redundancy_ms": ms_ap, "ratio": ms_ap / ms_pass,
+           "all_pairs_roofline": {"bound": "tensor", "achieved": flops / ms_ap / 1e9, "peak": tpeak,
+                                  "unit": "TFLOP/s", "frac": flops / ms_ap / 1e9 / tpeak, "peak_kind": tkind,
+                                  "flops_per_launch": flops}}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,10 +572,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--requests", type=int, default=0, help="override the workload's request count (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
+    ap.add_argument("--ablation", choices=["all_pairs"], default=None,
+                    help="time the original all-pairs redundancy against the fused Lightning pass")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.ablation:
+        run_ablation(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.workload == "mixed":
         run_mixed(args)

@@ -140,6 +140,34 @@ zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const
 size_t zp_compress_workspace_size(const zp_params* params, int32_t num_requests);
 
 /* ---------------------------------------------------------------------------------------
+ * Original (all-pairs) redundancy score — the ablation of the Lightning Redundancy Score
+ * (zh §2.1 and es §2: the original compares every pair of the N*b cached tokens, O(N^2 b^2),
+ * where Lightning compares the b^2 pairs of each block, O(N b^2); de §2: the original needs
+ * the full similarity matrix).  Not used by zp_compress: it exists to measure what Lightning
+ * saves.
+ *   redund[r][l][h][t] = (1/(L-1)) * sum over j < L, j != t of cos(k_t, k_j),
+ * cosine with norms clamped at 1e-12, for t < L = seq_len[r]; 0 for t >= L and when L < 2.
+ * Arguments
+ *   pool          device KV pool, read through block_tables (only K is read).
+ *   block_tables  device [R][max_blocks] int32.
+ *   meta          host struct: num_requests, max_blocks, seq_len (device [R]) and
+ *                 max_seq_len (the row length L_max of redund; n_max*b when 0).  The other
+ *                 fields are ignored.  L_max <= 4096.
+ *   params        host; num_layers, num_kv_heads, head_dim (64 or 128), block_size (16 or
+ *                 32) and n_max are used.
+ *   redund        device fp32 [R][num_layers][H_kv][L_max], written.
+ *   workspace     device, >= zp_redundancy_workspace_size() bytes, 256-byte aligned; holds
+ *                 the error word (a block id outside the pool or a seq_len above L_max:
+ *                 ZP_ERR_BAD_TABLE; a wait that gave up: ZP_ERR_TIMEOUT).
+ * Returns ZP_OK once queued.
+ * --------------------------------------------------------------------------------------- */
+zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
+                                  const zp_params* params, float* redund, void* workspace,
+                                  size_t workspace_bytes, zp_stream stream);
+
+size_t zp_redundancy_workspace_size(void);
+
+/* ---------------------------------------------------------------------------------------
  * Paged decode attention over the (compacted) cache — the consumer that runs on the main
  * stream while compression runs on a side stream (zh §2.1 asynchronous compression and
  * decoding; fr §2.D).

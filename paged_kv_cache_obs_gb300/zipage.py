@@ -85,6 +85,9 @@ _sig("zp_paged_decode_attn", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P
 _sig("zp_paged_decode_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_paged_decode_attn_static", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                            ctypes.POINTER(zp_params), _P, _P])
+_sig("zp_redundancy_all_pairs", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta),
+                                       ctypes.POINTER(zp_params), _P, _P, _SZ, _P])
+_sig("zp_redundancy_workspace_size", _SZ, [])
 _sig("zp_read_error", _I32, [_P, _P, _I32P])
 _sig("zp_alloc_create", _I32, [_I64, ctypes.POINTER(_P)])
 _sig("zp_alloc_destroy", None, [_P])
@@ -189,6 +192,25 @@ def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_sc
                          ctypes.byref(dbg) if dbg is not None else None, _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check("zp_compress", st)
+
+
+# ------------------------------------------------------------------ all-pairs redundancy -----
+
+def zp_redundancy_workspace_size() -> int:
+    return lib.zp_redundancy_workspace_size()
+
+
+def zp_redundancy_all_pairs(pool, block_tables, seq_len, redund, params: dict, workspace, stream=None,
+                            max_seq_len: int = 0):
+    """Queues the original all-pairs redundancy (the Lightning ablation) into redund
+    [R][layers][H_kv][L_max] fp32 (see include/zipage.h)."""
+    kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    meta = zp_seq_meta(block_tables.shape[0], block_tables.shape[1], seq_len.data_ptr(), None, None,
+                       max_seq_len, None)
+    st = lib.zp_redundancy_all_pairs(ctypes.byref(kv), _ptr(block_tables), ctypes.byref(meta),
+                                     ctypes.byref(make_params(params)), _ptr(redund), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("zp_redundancy_all_pairs", st)
 
 
 # ------------------------------------------------------------------ decode attention ---------
