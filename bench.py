@@ -322,9 +322,12 @@ def _ncu_traffic(workload):
 
 
 def run_e2e(args, wl, inp, pristine_pool, pristine_gs, world):
-    """Same metric through the public API with HOST buffers: every step copies the pool,
-    window queries, global scores and tables from pinned host memory, plans on the host,
-    compresses, and copies the compacted pool and global scores back to pinned host memory."""
+    """Same metric through the public API with HOST buffers.  Every step copies the window
+    queries, global scores and tables from pinned host memory, plans on the host, and then
+    streams the pool through the GPU a few layers at a time: the host-to-device copy of one
+    chunk of layers, the compression of the previous chunk (zp_compress over that layer range)
+    and the device-to-host copy of the chunk before it run on three streams at once (the link
+    is full duplex).  The compacted pool and global scores end in pinned host memory."""
     import numpy as np
     import torch
     from paged_kv_cache_obs_gb300 import runner, zipage
@@ -336,30 +339,55 @@ def run_e2e(args, wl, inp, pristine_pool, pristine_gs, world):
     h_gs_out = torch.empty_like(h_gs, pin_memory=True)
     h_tables = torch.from_numpy(inp.block_tables[:inp.num_compress].copy()).pin_memory()
     batch = runner.CompressionBatch(inp, "cuda", pool=torch.empty_like(pristine_pool))
-    stream = torch.cuda.Stream()
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    nl = wl.num_layers
+    per = max(1, nl // 16)  # layers per chunk
+    chunks = [(c, min(per, nl - c)) for c in range(0, nl, per)]
+    ws = [zipage.new_workspace(zipage.zp_compress_workspace_size(batch.params, inp.num_compress))
+          for _ in chunks]  # one error word per call
     steps = max(2, min(args.steps, 5))
     bytes_in = (h_pool.numel() * 2 + h_q.numel() * 2 + h_gs.numel() * 4 + 2 * h_tables.numel() * 4
                 + 2 * inp.num_compress * 4)
     bytes_out = h_pool.numel() * 2 + h_gs.numel() * 4
 
     def step():
-        with torch.cuda.stream(stream):
-            batch.pool.copy_(h_pool, non_blocking=True)
+        with torch.cuda.stream(s_in):
             batch.obs_q.copy_(h_q, non_blocking=True)
             batch.gs.copy_(h_gs, non_blocking=True)
             batch.d_tables.copy_(h_tables, non_blocking=True)
-            _reset_alloc(batch, inp)
-            batch.d_dst.copy_(torch.from_numpy(batch.dst_tables), non_blocking=False)
-            batch.launch(stream=stream)
-            batch.commit(stream=stream)
-            h_out.copy_(batch.pool, non_blocking=True)
+        _reset_alloc(batch, inp)
+        with torch.cuda.stream(s_in):
+            batch.d_dst.copy_(torch.from_numpy(batch.dst_tables).pin_memory(), non_blocking=True)
+        done = []
+        for i, (l0, n) in enumerate(chunks):
+            with torch.cuda.stream(s_in):
+                batch.pool[l0:l0 + n].copy_(h_pool[l0:l0 + n], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            s_comp.wait_event(ev_in)
+            batch.workspace = ws[i]
+            with torch.cuda.stream(s_comp):
+                batch.launch(stream=s_comp, layers=(l0, n))
+                ev_c = torch.cuda.Event()
+                ev_c.record(s_comp)
+            s_out.wait_event(ev_c)
+            with torch.cuda.stream(s_out):
+                h_out[l0:l0 + n].copy_(batch.pool[l0:l0 + n], non_blocking=True)
+            done.append(ev_c)
+        with torch.cuda.stream(s_comp):
+            batch.commit(stream=s_comp)
+        s_out.wait_stream(s_comp)
+        with torch.cuda.stream(s_out):
             h_gs_out.copy_(batch.gs, non_blocking=True)
-        stream.synchronize()
+        s_out.synchronize()
+        s_comp.synchronize()
         zipage.zp_alloc_drain(batch.alloc)
         zipage.zp_alloc_destroy(batch.alloc)
         batch.alloc = None
 
     step()
+    for w_ in ws:
+        assert zipage.zp_read_error(w_) == 0
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
@@ -369,7 +397,8 @@ def run_e2e(args, wl, inp, pristine_pool, pristine_gs, world):
     dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
     comp = inp.num_compress * wl.num_layers * world
     return {"value": comp / dt, "unit": "compressions/s", "h2d_bytes_per_step": int(bytes_in),
-            "d2h_bytes_per_step": int(bytes_out), "steps": steps, "ms_per_step": dt * 1e3}
+            "d2h_bytes_per_step": int(bytes_out), "steps": steps, "ms_per_step": dt * 1e3,
+            "pipeline": f"{len(chunks)} chunks of {per} layers: copy in, compress, copy out on three streams"}
 
 
 def run_cpu_baseline(inp, pool, gs):

@@ -91,6 +91,13 @@ typedef struct zp_seq_meta {
                                    2 <= N_max_r <= params.n_max (the pages' per-request dynamic
                                    budgets, de §5); request r keeps k_r = (N_max_r-1)*b tokens per
                                    head.  NULL: every request uses params.n_max. */
+  int32_t layer_begin;        /* the call compresses layers [layer_begin, layer_begin +
+                                 layer_count) of every request; layer_count 0 means all layers
+                                 (then layer_begin must be 0).  Layer indices into the pool,
+                                 obs_q, global_scores and the zp_debug arrays stay absolute, so a
+                                 caller can compress a model layer by layer (for instance while
+                                 the next layer's blocks are still being copied in). */
+  int32_t layer_count;
 } zp_seq_meta;
 
 /* Optional per-token outputs, each device [R][num_layers][num_kv_heads][L_max] (row-major),

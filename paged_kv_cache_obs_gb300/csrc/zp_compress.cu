@@ -62,6 +62,7 @@ struct CompressArgs {
   float* dbg_score;
   int32_t* dbg_keep;
   int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, max_blocks, num_qslots;  // L: launch length
+  int layer0, nl;                 // the call's layers: [layer0, layer0 + nl) of the `layers`
   float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
   float inv_rw;                   // 1 / (w * G_q)
   uint32_t block_bytes;           // bytes of one (layer, block): 2 * Hkv * b * d * 2
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int nblk_l = (nk_l + bm) >> bs;                // blocks loaded (a partial last block whole)
   const int n_mma = (nk_l + 15) & ~15;                 // MMA N over those keys
   const int nhalf = d / 64;
-  const int num_units = a.R * a.layers * a.Hkv;
+  const int num_units = a.R * a.nl * a.Hkv;
   const int cluster_id = static_cast<int>(blockIdx.x) / C;  // the C CTAs of a cluster are consecutive in x
   const int num_clusters = static_cast<int>(gridDim.x) / C;
 
@@ -299,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   int iter = 0;
   for (int unit = cluster_id; unit < num_units; ++iter) {
   const int h = unit % a.Hkv;
-  const int r = unit / a.Hkv / a.layers;
-  const int layer = (unit / a.Hkv) % a.layers;
+  const int r = unit / a.Hkv / a.nl;
+  const int layer = a.layer0 + (unit / a.Hkv) % a.nl;
   uint8_t* const head_base = a.pool + static_cast<size_t>(layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
                              static_cast<size_t>(h) * b * a.row_bytes;
 
@@ -813,6 +814,12 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
             b = p->block_size, n_max = p->n_max, w = p->window, R = meta->num_requests;
   if (layers <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || R < 0 || num_qslots <= 0) return ZP_ERR_INVALID_ARG;
   if (n_max < 2 || meta->max_blocks < n_max || w < 1) return ZP_ERR_INVALID_ARG;
+  // the call's layers (all of them unless a range is given)
+  const int layer_begin = meta->layer_count > 0 ? meta->layer_begin : 0;
+  const int nl = meta->layer_count > 0 ? meta->layer_count : layers;
+  if (meta->layer_count < 0 || (meta->layer_count == 0 && meta->layer_begin != 0) || layer_begin < 0 ||
+      layer_begin + nl > layers)
+    return ZP_ERR_INVALID_ARG;
   const int k = (n_max - 1) * b, Gq = Hq / Hkv, Rw = w * Gq;
   // launch length: the longest request of the call (n_max*b unless the caller says more)
   const int L = meta->max_seq_len > 0 ? meta->max_seq_len : n_max * b;
@@ -863,6 +870,8 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   }
   a.R = R;
   a.layers = layers;
+  a.layer0 = layer_begin;
+  a.nl = nl;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.d = d;
@@ -897,7 +906,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
 
   const int C = (L + kKeysPerCta - 1) / kKeysPerCta;
-  const int64_t num_units = static_cast<int64_t>(R) * layers * Hkv;
+  const int64_t num_units = static_cast<int64_t>(R) * nl * Hkv;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -58,10 +58,11 @@ class CompressionBatch:
                       "keep": z(torch.int32)}
         return self.debug
 
-    def launch(self, stream=None):
+    def launch(self, stream=None, layers=None):
+        """Queues the pass (over `layers` = (begin, count) only, when given)."""
         zipage.zp_compress(self.pool, self.d_tables, self.d_seq, self.d_qslot, self.d_dst, self.obs_q,
                            self.gs, self.params, self.workspace, debug=self.debug, stream=stream,
-                           max_seq_len=self.max_seq_len, n_max_per_req=self.d_nmax)
+                           max_seq_len=self.max_seq_len, n_max_per_req=self.d_nmax, layers=layers)
 
     def error(self, stream=None) -> int:
         return zipage.zp_read_error(self.workspace, stream)

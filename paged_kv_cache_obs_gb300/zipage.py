@@ -55,7 +55,8 @@ class zp_seq_meta(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("seq_len", ctypes.c_void_p), ("qslot", ctypes.c_void_p),
                 ("dst_tables", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
-                ("n_max_per_req", ctypes.c_void_p)]
+                ("n_max_per_req", ctypes.c_void_p), ("layer_begin", ctypes.c_int32),
+                ("layer_count", ctypes.c_int32)]
 
 
 class zp_debug(ctypes.Structure):
@@ -175,14 +176,17 @@ def zp_compress_workspace_size(params: dict, num_requests: int) -> int:
 
 
 def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_scores, params: dict,
-                workspace, debug: dict | None = None, stream=None, max_seq_len: int = 0, n_max_per_req=None):
+                workspace, debug: dict | None = None, stream=None, max_seq_len: int = 0, n_max_per_req=None,
+                layers: tuple | None = None):
     """Queues the compression pass; tensors are device tensors (see include/zipage.h).
     max_seq_len: the longest seq_len of the call (0: every request holds n_max*b tokens).
-    n_max_per_req: optional device int32 [R] of per-request block budgets."""
+    n_max_per_req: optional device int32 [R] of per-request block budgets.
+    layers: optional (layer_begin, layer_count) to compress only those layers."""
     kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    lb, lc = layers if layers is not None else (0, 0)
     meta = zp_seq_meta(block_tables.shape[0], block_tables.shape[1], seq_len.data_ptr(),
                        qslot.data_ptr(), dst_tables.data_ptr(), max_seq_len,
-                       None if n_max_per_req is None else n_max_per_req.data_ptr())
+                       None if n_max_per_req is None else n_max_per_req.data_ptr(), lb, lc)
     dbg = None
     if debug:
         dbg = zp_debug(*(debug[k].data_ptr() if debug.get(k) is not None else None

@@ -251,3 +251,26 @@ def test_full_size_sampled_units_and_properties(zp, name):
         sb = torch.tensor(shared, device="cuda")
         assert torch.equal(pristine[:, sb].view(torch.int16), batch.pool[:, sb].view(torch.int16))
     batch.close()
+
+
+def test_layer_by_layer_equals_one_call(zp):
+    """Compressing the layers one call at a time, in any order, gives the same bytes as one
+    call over every layer (units are independent; the one-call pass is checked against the
+    oracle by the tests above)."""
+    zipage, runner = zp
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=4)
+    inp = synth.make_inputs(wl, "cpu", seed=77)
+    whole = runner.CompressionBatch(inp, "cuda")
+    whole.launch()
+    assert whole.error() == 0
+    parts = runner.CompressionBatch(inp, "cuda")
+    for layer in (2, 0, 3, 1):
+        parts.launch(layers=(layer, 1))
+        assert parts.error() == 0
+    torch.cuda.synchronize()
+    assert torch.equal(parts.pool.view(torch.int16), whole.pool.view(torch.int16))
+    assert torch.equal(parts.gs, whole.gs)
+    with pytest.raises(zipage.ZipageError):
+        parts.launch(layers=(3, 2))  # past the last layer
+    whole.close()
+    parts.close()
