@@ -203,7 +203,7 @@ size_t zp_paged_decode_workspace_size(const zp_params* params, int32_t B, int32_
  * Same operation and arguments as zp_paged_decode_attn, except that the split-KV partials
  * live in a fixed 16 MiB array inside the library (held by every GPU that loads it until the
  * process exits), so no workspace is passed.  A call needs
- * B * H_q * ceil(max_blocks / 16) * (head_dim + 2) * 4 bytes of it, at most 16 MiB - 256 B;
+ * B * H_q * ceil(max_blocks / 32) * (head_dim + 2) * 4 bytes of it, at most 16 MiB - 256 B;
  * larger calls return ZP_ERR_TOO_LARGE and launch nothing.
  *   dev_status  device int32 written with the call's device-side status (0, or
  *               ZP_ERR_BAD_TABLE for a block id outside the pool or a bad seq_len); it is

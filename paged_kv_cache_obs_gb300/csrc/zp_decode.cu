@@ -7,13 +7,16 @@
 //   out[r][qh] = sum_t softmax_t(scale * <q[r][qh], k_t>) v_t,  t < seq_lens[r],
 // with k_t, v_t of kv head qh / G_q read through block_tables[r].
 //
-// Split-KV flash decoding.  Grid (split, kv head, request); each CTA of 4 warps walks its
-// split's blocks (warp w takes blocks w, w+4, ...).  A token's 256-byte K row is spread over
-// d/8 lanes (16 bytes each), so one warp-wide 16-byte load covers 32*16 bytes of K; the G_q
-// query heads of the kv head share every K/V byte loaded.  Each lane group keeps an online
-// softmax (log2 domain) per query head; groups, then warps, are merged at the end.  With
-// more than one split the (max, sum, acc) partials go to the workspace and a second kernel
-// merges the splits.
+// Split-KV flash decoding on the warp-level tensor cores.  Grid (split of 32 blocks, kv head,
+// request); each CTA of 4 warps walks its split's blocks (warp w takes blocks w, w+4, ...).  A
+// warp streams its blocks in chunks of 16 rows through two shared-memory stages: TMA brings a
+// chunk's K rows and V rows (128-byte swizzle, completing on the stage's mbarrier) while the
+// warp computes on the other stage.  The G_q query heads of the kv head are the rows of an
+// m16n8k16 MMA (padded to 16): S = Q K^T from ldmatrix fragments of K, an online softmax per
+// row in the log2 domain, then O += P V with V fragments from ldmatrix.trans.  P enters the
+// MMA as a bf16 high part plus a bf16 remainder, which keeps about 16 bits of it; the exp-sum
+// uses the fp32 values.  Warps are merged at the end; with more than one split the
+// (max, sum, acc) partials go to the workspace and a second kernel merges the splits.
 #include "zp_internal.h"
 #include "zp_ptx.cuh"
 
@@ -24,7 +27,9 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kBlocksPerSplit = 16;  // KV blocks per CTA
+constexpr int kBlocksPerSplit = 32;  // KV blocks per CTA (<= 32 * kWarps)
+constexpr int kChunkRows = 16;       // rows per bulk-copied K (and V) chunk: b = 16 or 32
+constexpr uint64_t kWaitNsD = 2000000000ull;
 
 struct DecodeArgs {
   const uint8_t* pool;
@@ -45,8 +50,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint16_t f2bf16(float f) {
   // round to nearest even; NaN stays NaN
@@ -56,26 +59,54 @@ __device__ __forceinline__ uint16_t f2bf16(float f) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+// Packs two floats into a bf16x2 register (lo in the low half), rounding to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16x2_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16x2_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Byte offset, inside a (16-row, D-column) chunk stored as [d/64 half][16 rows][128 B] with the
+// 128-byte swizzle that TMA applies, of 16-byte column group `cg` (0 .. D/8-1) of row `row`.
+template <int D>
+__device__ __forceinline__ uint32_t swz_off(int row, int cg) {
+  return static_cast<uint32_t>((cg >> 3) * (kChunkRows * 128) + row * 128 + (((cg & 7) ^ (row & 7)) << 4));
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
-  constexpr int LPT = D / 8;        // lanes per token
-  constexpr int TPS = 32 / LPT;     // tokens per warp step
-  constexpr int kStepsPerChunk = (G <= 4) ? 8 : 4;  // 16-byte lane loads in flight per chunk
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tm, const DecodeArgs a) {
+  constexpr int NH = D / 64;                   // 64-column halves
+  constexpr int kChunkBytes = kChunkRows * D * 2;
+  constexpr int NT = D / 8;                    // n8 tiles of the output row
   __shared__ float sm_m[kWarps][G], sm_l[kWarps][G];
   __shared__ float sm_acc[kWarps][G][D];
   __shared__ int sm_bad;
+  __shared__ __align__(8) uint64_t sm_bar[kWarps][2];
+  // per warp, two stages of (K, V) chunks of kChunkRows rows in the TMA's 128-byte swizzle
+  // (dynamic shared memory, 1024-byte aligned below)
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* const kv_base =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
-  const int sub = lane % LPT;       // which 16-byte chunk of the row
-  const int grp = lane / LPT;       // which token of the step
+  const int fr = lane >> 2, q = lane & 3;      // mma fragment row (query head) and column pair
   const int seq = a.seq_lens[r];
   const int b = a.b;
+  const int cpb = b / kChunkRows;              // chunks per block
   const int nblk = (seq + b - 1) / b;
   const int blk0 = split * kBlocksPerSplit;
   const int blk1 = min(nblk, blk0 + kBlocksPerSplit);
 
   if (tid == 0) sm_bad = (seq < 1 || seq > a.max_blocks * b) ? 1 : 0;
+  if (lane == 0) {
+    mbar_init(&sm_bar[warp][0], 1);
+    mbar_init(&sm_bar[warp][1], 1);
+    fence_mbar_init();
+  }
+  if (tid == 0) prefetch_tensormap(&tm);
   __syncthreads();
   if (sm_bad) {
     if (tid == 0 && split == 0 && h == 0) atomicCAS(a.err, 0, ZP_ERR_BAD_TABLE);
@@ -83,131 +114,145 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
   }
   if (blk0 >= nblk) return;  // this split has no work (uniform over the CTA)
 
-  // query chunk of this lane, pre-scaled into the log2 domain
-  float qf[G][8];
+  // Q as mma A fragments (rows = the G query heads, padded to 16 with zeros): per k-step of 16
+  // columns, qa[ks][0] holds row fr, columns 16ks + 2q, +1 and qa[ks][1] columns 16ks + 8 + 2q, +1.
+  uint32_t qa[D / 16][2];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(r) * a.Hq + h * G + g) * D + sub * 8);
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      qf[g][2 * i] = bf16_lo(w4[i]) * a.sl2;
-      qf[g][2 * i + 1] = bf16_hi(w4[i]) * a.sl2;
+  for (int ks = 0; ks < D / 16; ++ks) {
+    qa[ks][0] = qa[ks][1] = 0u;
+    if (fr < G) {
+      const uint32_t* qrow =
+          reinterpret_cast<const uint32_t*>(a.q + (static_cast<int64_t>(r) * a.Hq + h * G + fr) * D);
+      qa[ks][0] = qrow[(16 * ks + 2 * q) >> 1];
+      qa[ks][1] = qrow[(16 * ks + 8 + 2 * q) >> 1];
     }
   }
-  float m[G], l[G], acc[G][8];
+  // running max (log2 domain), this thread's share of the exp-sum, and the output row fr at
+  // columns 8nt + 2q, +1 (o[nt][2], o[nt][3] belong to padding rows)
+  float m = -INFINITY, l = 0.0f;
+  float o[NT][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[g][i] = 0.0f;
-  }
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
 
+  // This warp's blocks are blk0 + warp + kWarps*i (i < nb); lane i holds the physical id of
+  // the i-th one (kBlocksPerSplit / kWarps <= 32), so issuing a copy needs no global load.
+  const int nb = (blk1 - blk0 - warp + kWarps - 1) / kWarps;  // may be <= 0
   const int32_t* table = a.tables + static_cast<int64_t>(r) * a.max_blocks;
-  const int64_t tile_elems = static_cast<int64_t>(b) * D;
-  bool bad = false;
-  for (int blk = blk0 + warp; blk < blk1; blk += kWarps) {
-    const int phys = table[blk];
-    if (phys < 0 || phys >= a.num_blocks) {
-      bad = true;
-      continue;
-    }
-    const uint16_t* kbase =
-        reinterpret_cast<const uint16_t*>(a.pool) +
-        ((static_cast<int64_t>(a.layer) * a.num_blocks + phys) * 2 * a.Hkv + h) * tile_elems;
-    const uint16_t* vbase = kbase + static_cast<int64_t>(a.Hkv) * tile_elems;
-    for (int t0 = 0; t0 < b; t0 += kStepsPerChunk * TPS) {
-      uint4 kr[kStepsPerChunk];
+  const int my_phys = (lane < nb) ? table[blk0 + warp + kWarps * lane] : 0;
+  const bool my_bad = lane < nb && (my_phys < 0 || my_phys >= a.num_blocks);
+  const bool bad = __any_sync(0xffffffffu, my_bad);
+  const int nch = bad ? 0 : nb * cpb;  // chunks of this warp (none if a block id is bad)
+  uint8_t* const wbuf = kv_base + warp * (2 * 2 * kChunkBytes);  // [stage][K|V][chunk]
+  // chunk c of this warp: rows [(c % cpb) * kChunkRows, +kChunkRows) of its (c / cpb)-th block;
+  // in the pool viewed as {d, 2*Hkv*b rows, layers*blocks}, K rows of head h start at h*b and
+  // V rows at (Hkv + h)*b
+  auto issue = [&](int c, int st) {
+    const int phys = __shfl_sync(0xffffffffu, my_phys, c / cpb);
+    if (lane == 0) {
+      uint64_t* bar = &sm_bar[warp][st];
+      const int row = h * b + (c % cpb) * kChunkRows, z = a.layer * static_cast<int>(a.num_blocks) + phys;
+      mbar_arrive_expect_tx(bar, 2u * kChunkBytes);
 #pragma unroll
-      for (int s = 0; s < kStepsPerChunk; ++s) {
-        const int t = t0 + s * TPS + grp;
-        kr[s] = (t < b) ? *reinterpret_cast<const uint4*>(kbase + static_cast<int64_t>(t) * D + sub * 8)
-                        : make_uint4(0, 0, 0, 0);
-      }
-      float sc[kStepsPerChunk][G];
-#pragma unroll
-      for (int s = 0; s < kStepsPerChunk; ++s) {
-        const uint32_t w4[4] = {kr[s].x, kr[s].y, kr[s].z, kr[s].w};
-        float kf[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          kf[2 * i] = bf16_lo(w4[i]);
-          kf[2 * i + 1] = bf16_hi(w4[i]);
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float p = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) p = fmaf(qf[g][i], kf[i], p);
-#pragma unroll
-          for (int off = LPT / 2; off >= 1; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-          const int tok = blk * b + t0 + s * TPS + grp;
-          sc[s][g] = (t0 + s * TPS + grp < b && tok < seq) ? p : -INFINITY;
-        }
-      }
-      uint4 vr[kStepsPerChunk];
-#pragma unroll
-      for (int s = 0; s < kStepsPerChunk; ++s) {
-        const int t = t0 + s * TPS + grp;
-        vr[s] = (t < b) ? *reinterpret_cast<const uint4*>(vbase + static_cast<int64_t>(t) * D + sub * 8)
-                        : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float cm = m[g];
-#pragma unroll
-        for (int s = 0; s < kStepsPerChunk; ++s) cm = fmaxf(cm, sc[s][g]);
-        if (cm == -INFINITY) continue;
-        const float corr = ex2(m[g] - cm);
-        m[g] = cm;
-        l[g] *= corr;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[g][i] *= corr;
-#pragma unroll
-        for (int s = 0; s < kStepsPerChunk; ++s) {
-          const float p = ex2(sc[s][g] - cm);
-          l[g] += p;
-          const uint32_t w4[4] = {vr[s].x, vr[s].y, vr[s].z, vr[s].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[g][2 * i] = fmaf(p, bf16_lo(w4[i]), acc[g][2 * i]);
-            acc[g][2 * i + 1] = fmaf(p, bf16_hi(w4[i]), acc[g][2 * i + 1]);
-          }
-        }
+      for (int hd = 0; hd < NH; ++hd) {
+        tma_load_3d(wbuf + (st * 2 + 0) * kChunkBytes + hd * kChunkRows * 128, &tm, bar, hd * 64, row, z);
+        tma_load_3d(wbuf + (st * 2 + 1) * kChunkBytes + hd * kChunkRows * 128, &tm, bar, hd * 64,
+                    a.Hkv * b + row, z);
       }
     }
+  };
+  // ldmatrix rows: lanes 0-7 / 8-15 / 16-23 / 24-31 address matrices 0..3 = (rows 0-7, group j),
+  // (rows 8-15, group j), (rows 0-7, group j+1), (rows 8-15, group j+1)
+  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lgrp = lane >> 4;
+  uint32_t ph = 0;  // phase bit of each stage's barrier
+  bool ok = true;
+  int c = 0;
+  if (nch > 0) issue(0, 0);
+  if (nch > 1) issue(1, 1);
+  for (; c < nch; ++c) {
+    const int st = c & 1;
+    bool w = true;
+    if (lane == 0) w = mbar_wait_bounded(&sm_bar[warp][st], (ph >> st) & 1u, kWaitNsD);
+    w = __shfl_sync(0xffffffffu, w, 0);
+    if (!w) {
+      ok = false;
+      break;
+    }
+    ph ^= 1u << st;
+    const uint32_t kbuf = smem_u32(wbuf + (st * 2 + 0) * kChunkBytes);
+    const uint32_t vbuf = smem_u32(wbuf + (st * 2 + 1) * kChunkBytes);
+    const int tok0 = (blk0 + warp + kWarps * (c / cpb)) * b + (c % cpb) * kChunkRows;  // first token
+
+    // S = Q K^T for the chunk's 16 tokens: n-tile 0 = tokens 0-7, n-tile 1 = tokens 8-15
+    float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t kf[4];
+      ldmatrix_x4(kbuf + swz_off<D>(lrow, 2 * ks + lgrp), kf);
+      const uint32_t aq[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+      mma_16816_bf16(s0, aq, kf[0], kf[2]);
+      mma_16816_bf16(s1, aq, kf[1], kf[3]);
+    }
+    // online softmax of row fr over the 16 tokens (this thread: tokens 2q, 2q+1, 8+2q, 9+2q)
+    const int t0 = tok0 + 2 * q;
+    float sv[4] = {(t0 < seq) ? s0[0] * a.sl2 : -INFINITY, (t0 + 1 < seq) ? s0[1] * a.sl2 : -INFINITY,
+                   (t0 + 8 < seq) ? s1[0] * a.sl2 : -INFINITY, (t0 + 9 < seq) ? s1[1] * a.sl2 : -INFINITY};
+    float cm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+    const float mn = fmaxf(m, cm);
+    if (mn != -INFINITY) {  // uniform over the quad; false only for a fully masked chunk
+      const float corr = ex2(m - mn);
+      m = mn;
+      l *= corr;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= corr;
+        o[nt][1] *= corr;
+      }
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        p[e] = ex2(sv[e] - mn);
+        l += p[e];
+      }
+      // P as A fragments, split into a bf16 high part and a bf16 remainder so that P V keeps
+      // about 16 bits of P (the exp-sum l uses the fp32 values)
+      const uint32_t h01 = pack_bf16x2(p[0], p[1]), h23 = pack_bf16x2(p[2], p[3]);
+      const uint32_t l01 = pack_bf16x2(p[0] - bf16x2_lo(h01), p[1] - bf16x2_hi(h01));
+      const uint32_t l23 = pack_bf16x2(p[2] - bf16x2_lo(h23), p[3] - bf16x2_hi(h23));
+      const uint32_t ph_[4] = {h01, 0u, h23, 0u}, pl_[4] = {l01, 0u, l23, 0u};
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {  // pairs of n-tiles: columns 16np .. 16np + 15
+        uint32_t vf[4];
+        ldmatrix_x4_trans(vbuf + swz_off<D>(lrow, 2 * np + lgrp), vf);
+        mma_16816_bf16(o[2 * np], ph_, vf[0], vf[1]);
+        mma_16816_bf16(o[2 * np], pl_, vf[0], vf[1]);
+        mma_16816_bf16(o[2 * np + 1], ph_, vf[2], vf[3]);
+        mma_16816_bf16(o[2 * np + 1], pl_, vf[2], vf[3]);
+      }
+    }
+    __syncwarp();  // every lane is done with stage st before it is refilled
+    if (c + 2 < nch) issue(c + 2, st);
+  }
+  // copies still in flight after a failed wait: wait for them (bounded) before the CTA ends
+  if (!ok) {
+    if (lane == 0)
+      for (int k = c; k < min(nch, c + 2); ++k) mbar_wait_bounded(&sm_bar[warp][k & 1], (ph >> (k & 1)) & 1u, kWaitNsD);
+    atomicCAS(a.err, 0, ZP_ERR_TIMEOUT);
   }
   if (bad) atomicCAS(a.err, 0, ZP_ERR_BAD_TABLE);
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
 
-  // merge the TPS token groups of the warp (same dims, different tokens)
-#pragma unroll
-  for (int off = 16; off >= LPT; off >>= 1) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
-      const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
-      const float mn = fmaxf(m[g], mo);
-      const float c0 = (m[g] == -INFINITY) ? 0.0f : ex2(m[g] - mn);
-      const float c1 = (mo == -INFINITY) ? 0.0f : ex2(mo - mn);
-      l[g] = l[g] * c0 + lo * c1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float ao = __shfl_xor_sync(0xffffffffu, acc[g][i], off);
-        acc[g][i] = acc[g][i] * c0 + ao * c1;
-      }
-      m[g] = mn;
+  if (fr < G) {
+    if (q == 0) {
+      sm_m[warp][fr] = m;
+      sm_l[warp][fr] = l;
     }
-  }
-  if (lane < LPT) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (lane == 0) {
-        sm_m[warp][g] = m[g];
-        sm_l[warp][g] = l[g];
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sm_acc[warp][g][sub * 8 + i] = acc[g][i];
+    for (int nt = 0; nt < NT; ++nt) {
+      sm_acc[warp][fr][8 * nt + 2 * q] = o[nt][0];
+      sm_acc[warp][fr][8 * nt + 2 * q + 1] = o[nt][1];
     }
   }
   __syncthreads();
@@ -265,20 +310,27 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
 }
 
 template <int D, int G>
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  decode_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kThreads, 0, st>>>(a);
+cudaError_t launch_decode(const CUtensorMap& tm, const DecodeArgs& a, cudaStream_t st) {
+  constexpr int kv_bytes = kWarps * 2 * 2 * kChunkRows * D * 2 + 1024;  // + alignment slack
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
+  });
+  if (attr != cudaSuccess) return attr;
+  decode_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kThreads, kv_bytes, st>>>(tm, a);
   if (a.max_splits > 1) decode_combine_kernel<D><<<dim3(a.Hq, a.B), D, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t dispatch_g(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t dispatch_g(const CUtensorMap& tm, const DecodeArgs& a, cudaStream_t st) {
   switch (a.Gq) {
-    case 1: return launch_decode<D, 1>(a, st);
-    case 2: return launch_decode<D, 2>(a, st);
-    case 4: return launch_decode<D, 4>(a, st);
-    case 7: return launch_decode<D, 7>(a, st);
-    case 8: return launch_decode<D, 8>(a, st);
+    case 1: return launch_decode<D, 1>(tm, a, st);
+    case 2: return launch_decode<D, 2>(tm, a, st);
+    case 4: return launch_decode<D, 4>(tm, a, st);
+    case 7: return launch_decode<D, 7>(tm, a, st);
+    case 8: return launch_decode<D, 8>(tm, a, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -327,7 +379,14 @@ zp_status decode_launch(const zp_kv_pool* pool, int32_t layer, const uint16_t* q
   a.max_splits = decode_max_splits(max_blocks);
   a.sl2 = p->scale * 1.4426950408889634f;
   if (B == 0) return ZP_OK;
-  const cudaError_t e = (a.d == 128) ? dispatch_g<128>(a, st) : dispatch_g<64>(a, st);
+  // the pool as {d, 2*Hkv*b rows per (layer, block), layers*num_blocks}; box = 16 rows of one
+  // (K or V, head) tile, 64 columns, 128-byte swizzle
+  CUtensorMap tm;
+  if (!encode_tmap_3d_bf16(&tm, pool->base, a.d, static_cast<uint64_t>(2) * a.Hkv * a.b,
+                           static_cast<uint64_t>(p->num_layers) * pool->num_blocks, static_cast<uint64_t>(a.d) * 2,
+                           static_cast<uint64_t>(2) * a.Hkv * a.b * a.d * 2, 64, kChunkRows, 1))
+    return ZP_ERR_CUDA;
+  const cudaError_t e = (a.d == 128) ? dispatch_g<128>(tm, a, st) : dispatch_g<64>(tm, a, st);
   return e == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
 }
 
