@@ -84,7 +84,7 @@ typedef struct zp_seq_meta {
   const int32_t* qslot;       /* device [R]: query slot of each request, 0 <= qslot < num_qslots */
   const int32_t* dst_tables;  /* device [R][max_blocks]: where survivors go; equals the source
                                  table except at target blocks (zp_plan_compress) */
-  int32_t max_seq_len;        /* L_max: the longest seq_len of the call (<= 2048), or 0 for
+  int32_t max_seq_len;        /* L_max: the longest seq_len of the call (<= 4096), or 0 for
                                  n_max*b.  It is also the row length of global_scores and of
                                  the zp_debug arrays. */
   const int32_t* n_max_per_req; /* device [R] or NULL: per-request block budgets

@@ -40,9 +40,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kKeysPerCta = 256;
 constexpr int kRows = 128;         // window rows, padded: MMA M of D1 and N of D2
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;    // CTAs per cluster: 8 (portable, 2 CTAs per SM) or 16 (1 per SM)
 constexpr int kMaxEvict = 32;      // E = L - k = b <= 32
-constexpr int kMaxTable = 128;     // n_max entries cached per request
+// table entries cached per request for a cluster of up to MAXC CTAs (256 keys each, b >= 16)
+constexpr int max_table(int maxc) { return maxc * (kKeysPerCta / 16); }
 constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 
@@ -72,26 +73,27 @@ struct CompressArgs {
   int protect_window, causal;
 };
 
-struct __align__(1024) Smem {
+template <int MAXC>
+struct __align__(1024) SmemT {
   uint8_t K[2][kKeysPerCta * 128];  // [d-half][row][128 B], 128-byte swizzle
   uint8_t Q[2][kRows * 128];
   union {
     float2 part[2][kRows];          // pass-1 (max, sum) per column half
-    unsigned long long lists[192];  // cluster-level merge of the eviction candidates
+    unsigned long long lists[(MAXC - 2) * 32];  // cluster-level merge of the eviction candidates
   } u0;
   union {
-    float2 recv[kMaxCluster][kRows];            // (max, sum) partials of every CTA
+    float2 recv[MAXC][kRows];                   // (max, sum) partials of every CTA
     struct {
       unsigned long long key[kKeysPerCta];      // eviction keys of this CTA
       unsigned long long wcand[kKeysPerCta];    // per-warp candidates
     } sel;
   } u1;
-  unsigned long long cand_recv[kMaxCluster * 32];  // sorted bottom-32 list of every CTA
-  int status_recv[kMaxCluster];
+  unsigned long long cand_recv[MAXC * 32];  // sorted bottom-32 list of every CTA
+  int status_recv[MAXC];
   float row_off[kRows];
   int evict_pos[kMaxEvict];
-  int src_tab[kMaxTable];
-  int dst_tab[kMaxTable];
+  int src_tab[max_table(MAXC)];
+  int dst_tab[max_table(MAXC)];
   int dst_of[kKeysPerCta];          // destination slot of each key that moves, else -1
   float inv_n[kKeysPerCta];         // reciprocal key norms (Gram diagonal)
   uint64_t bar_tma;
@@ -100,13 +102,14 @@ struct __align__(1024) Smem {
   uint64_t bar_rs;                  // row statistics of every CTA of the cluster have landed
   uint32_t tmem_base;
   int next_unit[2];                 // unit after the current one, pushed by cluster rank 0
-  int kept_recv[kMaxCluster];       // kept keys of every CTA (many-eviction path)
+  int kept_recv[MAXC];              // kept keys of every CTA (many-eviction path)
   int warp_kept[kThreads / 32];
 };
 
 // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA, plus the
 // 1 KB alignment slack of the dynamic allocation
-static_assert(sizeof(Smem) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "shared memory must allow two CTAs per SM");
+static_assert(sizeof(SmemT<8>) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "8-CTA clusters: two CTAs per SM");
+static_assert(sizeof(SmemT<16>) + 1024 <= 227 * 1024, "16-CTA clusters: one CTA per SM");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -248,9 +251,11 @@ __device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2]
   return mt ? (hf ? v11 : v10) : (hf ? v01 : v00);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+template <int MAXC>
+__global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
     compress_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                     const CompressArgs a) {
+  using Smem = SmemT<MAXC>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_max_r = a.n_max_req ? a.n_max_req[r] : a.n_max;
   // Every table entry the launch may use is loaded now, independently of L and of the budget,
   // so that these loads overlap the two above; only the request's own entries are checked.
-  const int nblk_a = (La + bm) >> bs;  // <= kMaxTable <= kThreads
+  const int nblk_a = (La + bm) >> bs;  // <= max_table(MAXC) <= kThreads
   const int sb = tid < nblk_a ? a.block_tables[static_cast<int64_t>(r) * a.max_blocks + tid] : 0;
   const int db = tid < a.n_max - 1 ? a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + tid] : 0;
   const int k_r = (n_max_r - 1) * b;                 // tokens this request keeps per head
@@ -648,22 +653,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     cluster_sync();  // every CTA's sorted list is complete
     if (!skip && key_valid) {
-      int pos[kMaxCluster];
-      uint32_t base[kMaxCluster];
+      int pos[MAXC];
+      uint32_t base[MAXC];
 #pragma unroll
-      for (int cc = 0; cc < kMaxCluster; ++cc) {
+      for (int cc = 0; cc < MAXC; ++cc) {
         pos[cc] = 0;
         base[cc] = mapa(smem_u32(lst), cc < C ? cc : 0);
       }
 #pragma unroll
       for (int step = kKeysPerCta / 2; step > 0; step >>= 1)
 #pragma unroll
-        for (int cc = 0; cc < kMaxCluster; ++cc)
+        for (int cc = 0; cc < MAXC; ++cc)
           if (cc < C && ld_cluster_u64(base[cc] + 8u * static_cast<uint32_t>(pos[cc] + step - 1)) < mykey)
             pos[cc] += step;
       int rank = 0;
 #pragma unroll
-      for (int cc = 0; cc < kMaxCluster; ++cc) rank += (cc < C) ? pos[cc] : 0;
+      for (int cc = 0; cc < MAXC; ++cc) rank += (cc < C) ? pos[cc] : 0;
       evicted = rank < E;
     }
     const int kept_cta = __syncthreads_count(!skip && key_valid && !evicted);
@@ -700,19 +705,32 @@ __global__ void __launch_bounds__(kThreads, 2)
       // cluster level: merge the C sorted lists (missing lists count as +inf), identically in
       // every CTA; the first E keys of the result are evicted.  Scratch in u0: the u1 buffers
       // may already receive the next unit's row statistics.
-      unsigned long long* const m4 = s.u0.lists;        // [4][32]
-      unsigned long long* const m2 = s.u0.lists + 128;  // [2][32]
-      if (warp < 4) {
+      // Pairwise tree: level 1 merges the MAXC lists into MAXC/2, ..., down to 2 lists, which
+      // warp 0 merges into the final one.
+      static_assert(MAXC == 8 || MAXC == 16, "merge tree of 8 or 16 lists");
+      unsigned long long* lvl = s.u0.lists;  // [MAXC/2][32], then [MAXC/4][32], ...
+      if (warp < MAXC / 2) {
         const unsigned long long x0 = (2 * warp < C) ? s.cand_recv[(2 * warp) * 32 + lane] : ~0ull;
         const unsigned long long x1 = (2 * warp + 1 < C) ? s.cand_recv[(2 * warp + 1) * 32 + lane] : ~0ull;
-        m4[warp * 32 + lane] = warp_merge_low32(x0, x1, lane);
+        lvl[warp * 32 + lane] = warp_merge_low32(x0, x1, lane);
       }
       __syncthreads();
-      if (warp < 2)
-        m2[warp * 32 + lane] = warp_merge_low32(m4[(2 * warp) * 32 + lane], m4[(2 * warp + 1) * 32 + lane], lane);
-      __syncthreads();
+      if constexpr (MAXC >= 16) {  // 8 lists -> 4
+        unsigned long long* const nxt = lvl + 8 * 32;
+        if (warp < 4)
+          nxt[warp * 32 + lane] = warp_merge_low32(lvl[(2 * warp) * 32 + lane], lvl[(2 * warp + 1) * 32 + lane], lane);
+        __syncthreads();
+        lvl = nxt;
+      }
+      {  // 4 lists -> 2
+        unsigned long long* const nxt = lvl + 4 * 32;
+        if (warp < 2)
+          nxt[warp * 32 + lane] = warp_merge_low32(lvl[(2 * warp) * 32 + lane], lvl[(2 * warp + 1) * 32 + lane], lane);
+        __syncthreads();
+        lvl = nxt;
+      }
       if (warp == 0) {
-        const unsigned long long fin = warp_merge_low32(m2[lane], m2[32 + lane], lane);
+        const unsigned long long fin = warp_merge_low32(lvl[lane], lvl[32 + lane], lane);
         if (lane < E) s.evict_pos[lane] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(fin & 0xFFFFFFFFu));
       }
       __syncthreads();
@@ -791,7 +809,61 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
-size_t compress_smem_bytes() { return sizeof(Smem) + 1024; }
+template <int MAXC>
+size_t compress_smem_bytes() { return sizeof(SmemT<MAXC>) + 1024; }
+
+// Launches the persistent clusters of compress_kernel<MAXC> (C <= MAXC CTAs each).
+template <int MAXC>
+zp_status launch_compress(const CUtensorMap& tmK, const CUtensorMap& tmQ, const CompressArgs& a, int C,
+                          int64_t num_units, cudaStream_t st) {
+  const size_t smem = compress_smem_bytes<MAXC>();
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(compress_kernel<MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    if (attr_err == cudaSuccess && MAXC > 8)
+      attr_err = cudaFuncSetAttribute(compress_kernel<MAXC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+  if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many clusters as are co-resident (persistent), never more than there are units
+  static std::mutex occ_mu;
+  static int occ_cache[64][MAXC + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZP_ERR_CUDA;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(occ_mu);
+    if (dev >= 0 && dev < 64 && occ_cache[dev][C] > 0) {
+      max_clusters = occ_cache[dev][C];
+    } else {
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, compress_kernel<MAXC>, &cfg) != cudaSuccess ||
+          max_clusters <= 0)
+        max_clusters = 1;
+      if (dev >= 0 && dev < 64) occ_cache[dev][C] = max_clusters;
+    }
+  }
+  // Units are handed out dynamically, so launching more clusters than can be resident only
+  // leaves the late ones an empty queue; MAXC <= 8 fits two CTAs per SM, 16 one.
+  const int per_sm = MAXC <= 8 ? 2 : 1;
+  const int64_t want = std::max<int64_t>(max_clusters, (per_sm * static_cast<int64_t>(num_sms())) / C);
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(num_units, want));
+  cfg.gridDim = dim3(static_cast<unsigned>(C * clusters), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, compress_kernel<MAXC>, tmK, tmQ, a) != cudaSuccess) return ZP_ERR_CUDA;
+  return ZP_OK;
+}
 
 }  // namespace zp
 
@@ -827,7 +899,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   if (meta->max_blocks < (L + b - 1) / b) return ZP_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ZP_ERR_UNSUPPORTED;
   if (b != 16 && b != 32) return ZP_ERR_UNSUPPORTED;
-  if (Rw > kRows || n_max > kMaxTable || (L + kKeysPerCta - 1) / kKeysPerCta > kMaxCluster)
+  if (Rw > kRows || n_max > max_table(kMaxCluster) || (L + kKeysPerCta - 1) / kKeysPerCta > kMaxCluster)
     return ZP_ERR_UNSUPPORTED;
   if (Gq > 256 || w > 256) return ZP_ERR_UNSUPPORTED;
   if (!aligned(pool->base, 16) || !aligned(obs_q, 16)) return ZP_ERR_INVALID_ARG;
@@ -896,50 +968,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.protect_window = p->protect_window;
   a.causal = p->causal;
 
-  const size_t smem = compress_smem_bytes();
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem));
-  });
-  if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
-
   const int C = (L + kKeysPerCta - 1) / kKeysPerCta;
   const int64_t num_units = static_cast<int64_t>(R) * nl * Hkv;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(C, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // as many clusters as are co-resident (persistent), never more than there are units
-  static std::mutex occ_mu;
-  static int occ_cache[64][kMaxCluster + 1] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ZP_ERR_CUDA;
-  int max_clusters = 0;
-  {
-    std::lock_guard<std::mutex> lock(occ_mu);
-    if (dev >= 0 && dev < 64 && occ_cache[dev][C] > 0) {
-      max_clusters = occ_cache[dev][C];
-    } else {
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, compress_kernel, &cfg) != cudaSuccess || max_clusters <= 0)
-        max_clusters = 1;
-      if (dev >= 0 && dev < 64) occ_cache[dev][C] = max_clusters;
-    }
-  }
-  // Units are handed out dynamically, so launching more clusters than can be resident only
-  // leaves the late ones an empty queue; two CTAs fit per SM.
-  const int64_t want = std::max<int64_t>(max_clusters, (2 * static_cast<int64_t>(num_sms())) / C);
-  const int64_t clusters = std::min<int64_t>(num_units, want);
-  cfg.gridDim = dim3(static_cast<unsigned>(C * clusters), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, compress_kernel, tmK, tmQ, a) != cudaSuccess) return ZP_ERR_CUDA;
-  return ZP_OK;
+  return C <= 8 ? launch_compress<8>(tmK, tmQ, a, C, num_units, st) : launch_compress<16>(tmK, tmQ, a, C, num_units, st);
 }

@@ -83,6 +83,13 @@ SMALL = {
     # clusters of 1..3 active CTAs under a launch of 3
     "budgets_small": synth.WORKLOADS["llama3_8b"].scaled(num_requests=5, num_layers=2, n_max=40, window=16,
                                                          budget_min=3),
+    # beyond one portable cluster: 16-CTA clusters (one CTA per SM).  A decode trigger at
+    # L = 3200 (13 CTAs, E = 16), and long prefills (L = 1171 .. 3824 in a launch of 16 CTAs,
+    # E up to 2816)
+    "long_trigger": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
+                                                        num_q_heads=8, n_max=200),
+    "long_prefill": synth.WORKLOADS["prefill"].scaled(num_requests=6, num_layers=1, num_kv_heads=2,
+                                                      num_q_heads=8, n_max=64, prefill_max=4000),
 }
 
 
