@@ -420,36 +420,9 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
     const int vlim = max(0, min(ncol, (a.causal ? (L - w + i / Gq) : (L - 1)) - t0 - cbase + 1));
     const int vall = max(0, min(ncol, (a.causal ? (L - w) : (L - 1)) - t0 - cbase + 1));
     const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col0 = c2 * 64;
-      if (col0 >= ncol) break;
-      uint32_t ra[32], rb[32];
-      tmem_ld32_issue(tl + col0, ra);
-      tmem_ld32_issue(tl + col0 + 32, rb);
-      tmem_wait_ld(ra);
-      tmem_ld_dep(rb);
-      if (col0 + 32 <= vall) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
-      } else {
-        const int lim = vlim - col0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < lim) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
-      }
-      if (col0 + 64 <= vall) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
-      } else {
-        const int lim = vlim - col0 - 32;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < lim) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
-      }
-    }
-    const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    const float mo = m * a.sl2;
+    // online over two 64-column chunks: the chunk's max, then its exponentials against the
+    // running max (the sum so far is rescaled when the max grows); one TMEM read per chunk
+    float m = -INFINITY;
     float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     for (int c2 = 0; c2 < 2; ++c2) {
       const int col0 = c2 * 64;
@@ -459,23 +432,49 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
       tmem_ld32_issue(tl + col0 + 32, rb);
       tmem_wait_ld(ra);
       tmem_ld_dep(rb);
-      if (col0 + 32 <= vall) {
+      const bool fa = col0 + 32 <= vall, fb = col0 + 64 <= vall;  // groups every row sees whole
+      const int la = vlim - col0, lb = vlim - col0 - 32;          // visible columns of each group
+      float mx[4] = {m, m, m, m};
+      if (fa) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < la) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+      }
+      if (fb) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < lb) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
+      }
+      const float mn = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      if (mn == -INFINITY) continue;  // nothing visible yet
+      if (m != -INFINITY && mn > m) {
+        const float corr = ex2((m - mn) * a.sl2);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ls[e] *= corr;
+      }
+      m = mn;
+      const float mo = m * a.sl2;
+      if (fa) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
       } else {
-        const int lim = vlim - col0;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j < lim) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
+          if (j < la) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
       }
-      if (col0 + 64 <= vall) {
+      if (fb) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
       } else {
-        const int lim = vlim - col0 - 32;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j < lim) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
+          if (j < lb) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
       }
     }
     // rows without a visible key keep m = -inf and l = 0; padding rows are dropped below
