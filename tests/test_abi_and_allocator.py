@@ -203,3 +203,29 @@ def test_plan_and_commit_with_per_request_budgets(zp):
             zp.zp_plan_compress_budgets(a, tables, [1, 5])  # a budget below 2
     finally:
         zp.zp_alloc_destroy(a)
+
+
+def test_host_validation_of_layer_ranges_and_all_pairs(zp):
+    """Argument checks that return before any device work (no GPU needed): a layer range past
+    the last layer, a negative count, a begin without a count; and the all-pairs redundancy's
+    unsupported head sizes and lengths."""
+    import ctypes
+    p = dict(num_layers=4, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, n_max=8,
+             window=8, alpha=0.5, beta=0.5, decay=0.9, scale=0.125, protect_window=1, causal=1)
+    fake = 1 << 20  # never dereferenced: the calls fail before touching device memory
+    kv = zp.zp_kv_pool(fake, 64)
+    params = zp.make_params(p)
+    for lb, lc in ((3, 2), (0, -1), (1, 0), (-1, 2)):
+        meta = zp.zp_seq_meta(1, 8, fake, fake, fake, 0, None, lb, lc)
+        st = zp.lib.zp_compress(ctypes.byref(kv), fake, ctypes.byref(meta), fake, 1, fake, ctypes.byref(params),
+                                None, fake, 256, None)
+        assert st == zp.ZP_ERR_INVALID_ARG, (lb, lc)
+    meta = zp.zp_seq_meta(1, 8, fake, None, None, 0, None, 0, 0)
+    bad_d = zp.make_params(dict(p, head_dim=96))
+    assert zp.lib.zp_redundancy_all_pairs(ctypes.byref(kv), fake, ctypes.byref(meta), ctypes.byref(bad_d), fake,
+                                          fake, 256, None) == zp.ZP_ERR_UNSUPPORTED
+    long_meta = zp.zp_seq_meta(1, 400, fake, None, None, 5000, None, 0, 0)
+    assert zp.lib.zp_redundancy_all_pairs(ctypes.byref(kv), fake, ctypes.byref(long_meta), ctypes.byref(params),
+                                          fake, fake, 256, None) == zp.ZP_ERR_UNSUPPORTED
+    assert zp.lib.zp_redundancy_all_pairs(ctypes.byref(kv), fake, ctypes.byref(meta), ctypes.byref(params),
+                                          fake, fake, 8, None) == zp.ZP_ERR_INVALID_ARG  # workspace too small
