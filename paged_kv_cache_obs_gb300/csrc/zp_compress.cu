@@ -2,30 +2,32 @@
 //
 // Operation (Zipage summaries on gist.science: zh §2.1 core mechanism and Lightning Redundancy
 // Score, zh §2.2 prefix-cache compatibility, zh §2.3 cross-layer parallel compression, fr §2.A
-// window always kept).  Per unit u = (request r, layer l, kv head h) with L = n_max*b cached
-// tokens:
+// window always kept).  Per unit u = (request r, layer l, kv head h) with L cached tokens
+// (L = n_max*b at the decode trigger, more after a long prefill) and k = (n_max-1)*b:
 //   attn[t] = mean_{rows (i,g)} softmax_t(scale*<q_{i,g}, k_t>)   (row i = position L-w+i)
 //   R[t]    = mean_{j in block(t), j != t} cos(k_t, k_j)           (Lightning redundancy)
 //   S[t]    = attn[t] + alpha*G[t] - beta*R[t]                     (+inf on the protected window)
-//   keep the k = (n_max-1)*b best (S desc, t asc), copy survivor j to slot j of the dst table,
+//   keep the k best (S desc, t asc), copy survivor j to slot j of the dst table,
 //   G'[j] = decay*G[src_j] + attn[src_j], G'[k..L) = 0.
 //
-// GB300 mapping.  One thread-block cluster of C = ceil(L/256) CTAs per unit; CTA c owns the
-// 256 logical slots [256c, 256c+256).  Each CTA:
+// GB300 mapping.  Persistent thread-block clusters of C = ceil(L/256) CTAs (up to 8 at two
+// CTAs per SM, up to 16 at one) take units from a global counter; CTA c owns the 256 logical
+// slots [256c, 256c+256).  Per unit each CTA:
 //   1. TMA-loads its K rows (paged gather: one 3-D box per (block, 64-column half)) and the
 //      unit's w*G_q window queries into 128-byte-swizzled shared memory.
 //   2. tcgen05 MMA D1 = Q K^T (M=128 query rows, N=256 keys) into TMEM; each thread owns one
-//      query row and reduces its row max / exp-sum without shuffles.
-//   3. Pushes the per-row (max, sum) partials to every CTA of the cluster (DSMEM); meanwhile
-//      MMA Gram = K_h K_h^T per 128-key half gives the in-block cosine similarities
-//      (Lightning redundancy, diagonal = squared norms).
+//      query row and reduces its row max / exp-sum without shuffles (pass 1).
+//   3. Sends the per-row (max, sum) partials to every CTA of the cluster as st.async stores
+//      counted on the receiver's mbarrier; meanwhile each warp computes the Lightning
+//      redundancy of its 32 keys with warp-level MMA (block Gram, diagonal = squared norms).
 //   4. MMA D2 = K Q^T (M=128 keys, N=128 rows): each thread owns one key and sums its
-//      normalised probabilities over the window rows without shuffles.
-//   5. Selection: per-warp, per-CTA and per-cluster candidate filtering of the E = L-k
-//      lowest (S asc, t desc) keys; every CTA derives the same eviction set.
-//   6. V rows that move are loaded into registers; a cluster barrier separates every read of
-//      the unit from every write (compaction is in place, dst <= src); K rows are written
-//      from shared memory, V rows from registers, G' from registers.
+//      normalised probabilities over the window rows without shuffles (pass 2).
+//   5. Selection of the E = L-k lowest (S asc, t desc) keys: per-warp bitonic sort and merge
+//      trees (E <= 32) or a shared-memory sort and DSMEM ranks (E > 32); every CTA derives the
+//      same eviction set.
+//   6. V rows are staged (shared memory and registers) before a cluster barrier that separates
+//      every read of the unit from every write (compaction is in place, dst <= src); K rows are
+//      written from shared memory, V rows from the staging, G' from registers.
 // All waits are bounded; a failed wait or a bad table makes the whole unit skip its writes.
 #include <cstdio>
 #include <algorithm>
