@@ -550,7 +550,7 @@ def run_ablation(args):
     R = inp.num_compress
     L = batch.max_seq_len or wl.L
     redund = torch.empty((R, wl.num_layers, wl.num_kv_heads, L), device="cuda")
-    ws = zipage.new_workspace(zipage.zp_redundancy_workspace_size())
+    ws = zipage.new_workspace(zipage.zp_redundancy_workspace_size(p, R, batch.max_seq_len))
 
     def timed(fn):
         ts = []

@@ -163,16 +163,19 @@ size_t zp_compress_workspace_size(const zp_params* params, int32_t num_requests)
  *   params        host; num_layers, num_kv_heads, head_dim (64 or 128), block_size (16 or
  *                 32) and n_max are used.
  *   redund        device fp32 [R][num_layers][H_kv][L_max], written.
- *   workspace     device, >= zp_redundancy_workspace_size() bytes, 256-byte aligned; holds
- *                 the error word (a block id outside the pool or a seq_len above L_max:
- *                 ZP_ERR_BAD_TABLE; a wait that gave up: ZP_ERR_TIMEOUT).
+ *   workspace     device, >= zp_redundancy_workspace_size(params, R, max_seq_len) bytes,
+ *                 256-byte aligned: the error word (a block id outside the pool or a seq_len
+ *                 above L_max: ZP_ERR_BAD_TABLE; a wait that gave up: ZP_ERR_TIMEOUT), then
+ *                 the squared key norms that a pre-pass computes.
  * Returns ZP_OK once queued.
  * --------------------------------------------------------------------------------------- */
 zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
                                   const zp_params* params, float* redund, void* workspace,
                                   size_t workspace_bytes, zp_stream stream);
 
-size_t zp_redundancy_workspace_size(void);
+/* Bytes of workspace zp_redundancy_all_pairs needs: the error word and one fp32 squared key
+ * norm per (request, layer, kv head, token < L_max). */
+size_t zp_redundancy_workspace_size(const zp_params* params, int32_t num_requests, int32_t max_seq_len);
 
 /* ---------------------------------------------------------------------------------------
  * Paged decode attention over the (compacted) cache — the consumer that runs on the main

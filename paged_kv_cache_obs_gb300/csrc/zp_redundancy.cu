@@ -35,6 +35,7 @@ struct ApArgs {
   const int32_t* block_tables;
   const int32_t* seq_len;
   float* out;
+  float* sq;                      // [units][L] squared key norms (workspace), from the pre-pass
   int32_t* err;
   int layers, Hkv, d, b, b_shift, max_blocks, L, nt;  // L: launch length, nt: row tiles per unit
 };
@@ -50,24 +51,6 @@ struct __align__(1024) ApSmem {
 
 __device__ __forceinline__ void ap_record_error(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
-}
-
-// Squared norm of row `row` of a swizzled [half][row][128 B] tile, in fp32.
-__device__ __forceinline__ float row_sq_norm(const uint8_t (&T)[2][kTile * 128], int row, int nhalf) {
-  float acc = 0.0f;
-  for (int hd = 0; hd < nhalf; ++hd)
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      const uint4 v = *reinterpret_cast<const uint4*>(&T[hd][row * 128 + ((ch ^ (row & 7)) << 4)]);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
-        acc = fmaf(lo, lo, acc);
-        acc = fmaf(hi, hi, acc);
-      }
-    }
-  return acc;
 }
 
 // Zeroes row `row` of a swizzled tile (rows past the sequence must not contribute).
@@ -88,6 +71,37 @@ __device__ __forceinline__ void load_tile(uint8_t (&dst)[2][kTile * 128], const 
   for (int bi = 0; bi < nblk; ++bi)
     for (int hd = 0; hd < nhalf; ++hd)
       tma_load_3d(&dst[hd][bi * a.b * 128], tm, bar, hd * 64, h * a.b, layer * a.num_blocks + tab[blk0 + bi]);
+}
+
+// Pre-pass: the squared norm of every key of every unit (t < L; 0 past it), in fp32, read once
+// from the pool through the block table.  Grid (unit, 128-row tile), thread = key.
+__global__ void __launch_bounds__(kThreadsA) key_sq_norm_kernel(const ApArgs a) {
+  const int tid = threadIdx.x;
+  const int unit = static_cast<int>(blockIdx.x) / a.nt, it = static_cast<int>(blockIdx.x) % a.nt;
+  const int h = unit % a.Hkv, layer = (unit / a.Hkv) % a.layers, r = unit / a.Hkv / a.layers;
+  const int t = it * kTile + tid;
+  if (t >= a.L) return;
+  const int L = a.seq_len[r];
+  float acc = 0.0f;
+  if (L >= 0 && L <= a.L && t < L) {
+    const int phys = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + (t >> a.b_shift)];
+    if (phys >= 0 && phys < a.num_blocks) {  // bad ids are reported by the main kernel
+      const uint4* row = reinterpret_cast<const uint4*>(
+          a.pool + ((static_cast<int64_t>(layer) * a.num_blocks + phys) * 2 * a.Hkv + h) * static_cast<int64_t>(a.b) * a.d * 2 +
+          static_cast<int64_t>(t & (a.b - 1)) * a.d * 2);
+      for (int i = 0; i < a.d / 8; ++i) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+          acc = fmaf(lo, lo, acc);
+          acc = fmaf(hi, hi, acc);
+        }
+      }
+    }
+  }
+  a.sq[static_cast<int64_t>(unit) * a.L + t] = acc;
 }
 
 __global__ void __launch_bounds__(kThreadsA, 2)
@@ -150,9 +164,10 @@ __global__ void __launch_bounds__(kThreadsA, 2)
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
   float inv_a = 0.0f, self = 0.0f;
+  const float* const sq_unit = a.sq + static_cast<int64_t>(unit) * a.L;
   if (!fail) {
     if (t >= L) zero_row(s.A, tid, nhalf);
-    const float sq = t < L ? row_sq_norm(s.A, tid, nhalf) : 0.0f;
+    const float sq = t < L ? sq_unit[t] : 0.0f;
     inv_a = 1.0f / fmaxf(sqrtf(sq), 1e-12f);
     self = sq * inv_a * inv_a;  // cos(k_t, k_t): 1, or 0 for a zero key
   }
@@ -207,7 +222,7 @@ __global__ void __launch_bounds__(kThreadsA, 2)
     if (fail) break;
     const int tj = jt * kTile + tid;  // the key row this thread normalises
     if (tj >= L) zero_row(s.B[st], tid, nhalf);
-    s.inv_b[st][tid] = tj < L ? 1.0f / fmaxf(sqrtf(row_sq_norm(s.B[st], tid, nhalf)), 1e-12f) : 0.0f;
+    s.inv_b[st][tid] = tj < L ? 1.0f / fmaxf(sqrtf(sq_unit[tj]), 1e-12f) : 0.0f;
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -261,7 +276,12 @@ static_assert(sizeof(ApSmem) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "shared memo
 
 using namespace zp;
 
-extern "C" size_t zp_redundancy_workspace_size(void) { return 256; }
+extern "C" size_t zp_redundancy_workspace_size(const zp_params* p, int32_t num_requests, int32_t max_seq_len) {
+  if (!p || num_requests < 0) return 0;
+  const int64_t L = max_seq_len > 0 ? max_seq_len : static_cast<int64_t>(p->n_max) * p->block_size;
+  // error word, then the squared key norms of every unit
+  return 256 + static_cast<size_t>(num_requests) * p->num_layers * p->num_kv_heads * static_cast<size_t>(L) * 4;
+}
 
 extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32_t* block_tables,
                                              const zp_seq_meta* meta, const zp_params* p, float* redund,
@@ -271,7 +291,8 @@ extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32
   const int R = meta->num_requests;
   if (R < 0) return ZP_ERR_INVALID_ARG;
   if (R > 0 && (!block_tables || !meta->seq_len || !redund)) return ZP_ERR_INVALID_ARG;
-  if (workspace_bytes < zp_redundancy_workspace_size() || !aligned(workspace, 256)) return ZP_ERR_INVALID_ARG;
+  if (workspace_bytes < zp_redundancy_workspace_size(p, R, meta->max_seq_len) || !aligned(workspace, 256))
+    return ZP_ERR_INVALID_ARG;
   const int layers = p->num_layers, Hkv = p->num_kv_heads, d = p->head_dim, b = p->block_size;
   if (layers <= 0 || Hkv <= 0 || p->n_max < 1) return ZP_ERR_INVALID_ARG;
   const int L = meta->max_seq_len > 0 ? meta->max_seq_len : p->n_max * b;
@@ -303,6 +324,7 @@ extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32
   a.seq_len = meta->seq_len;
   a.out = redund;
   a.err = static_cast<int32_t*>(workspace);
+  a.sq = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
   a.layers = layers;
   a.Hkv = Hkv;
   a.d = d;
@@ -320,6 +342,7 @@ extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32
                                     static_cast<int>(smem));
   });
   if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
+  key_sq_norm_kernel<<<static_cast<unsigned>(ctas), kThreadsA, 0, st>>>(a);
   all_pairs_redundancy_kernel<<<static_cast<unsigned>(ctas), kThreadsA, smem, st>>>(tmK, a);
   return cudaGetLastError() == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
 }

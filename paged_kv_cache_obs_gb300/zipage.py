@@ -88,7 +88,7 @@ _sig("zp_paged_decode_attn_static", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P,
                                            ctypes.POINTER(zp_params), _P, _P])
 _sig("zp_redundancy_all_pairs", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta),
                                        ctypes.POINTER(zp_params), _P, _P, _SZ, _P])
-_sig("zp_redundancy_workspace_size", _SZ, [])
+_sig("zp_redundancy_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_read_error", _I32, [_P, _P, _I32P])
 _sig("zp_alloc_create", _I32, [_I64, ctypes.POINTER(_P)])
 _sig("zp_alloc_destroy", None, [_P])
@@ -200,8 +200,8 @@ def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_sc
 
 # ------------------------------------------------------------------ all-pairs redundancy -----
 
-def zp_redundancy_workspace_size() -> int:
-    return lib.zp_redundancy_workspace_size()
+def zp_redundancy_workspace_size(params: dict, num_requests: int, max_seq_len: int = 0) -> int:
+    return lib.zp_redundancy_workspace_size(ctypes.byref(make_params(params)), num_requests, max_seq_len)
 
 
 def zp_redundancy_all_pairs(pool, block_tables, seq_len, redund, params: dict, workspace, stream=None,

@@ -222,10 +222,13 @@ def test_host_validation_of_layer_ranges_and_all_pairs(zp):
         assert st == zp.ZP_ERR_INVALID_ARG, (lb, lc)
     meta = zp.zp_seq_meta(1, 8, fake, None, None, 0, None, 0, 0)
     bad_d = zp.make_params(dict(p, head_dim=96))
+    big = 1 << 30  # a workspace size that passes its check
     assert zp.lib.zp_redundancy_all_pairs(ctypes.byref(kv), fake, ctypes.byref(meta), ctypes.byref(bad_d), fake,
-                                          fake, 256, None) == zp.ZP_ERR_UNSUPPORTED
+                                          fake, big, None) == zp.ZP_ERR_UNSUPPORTED
     long_meta = zp.zp_seq_meta(1, 400, fake, None, None, 5000, None, 0, 0)
     assert zp.lib.zp_redundancy_all_pairs(ctypes.byref(kv), fake, ctypes.byref(long_meta), ctypes.byref(params),
-                                          fake, fake, 256, None) == zp.ZP_ERR_UNSUPPORTED
+                                          fake, fake, big, None) == zp.ZP_ERR_UNSUPPORTED
     assert zp.lib.zp_redundancy_all_pairs(ctypes.byref(kv), fake, ctypes.byref(meta), ctypes.byref(params),
-                                          fake, fake, 8, None) == zp.ZP_ERR_INVALID_ARG  # workspace too small
+                                          fake, fake, 256, None) == zp.ZP_ERR_INVALID_ARG  # workspace too small
+    # error word plus one fp32 squared norm per (request, layer, kv head, token)
+    assert zp.zp_redundancy_workspace_size(p, 3, 100) == 256 + 3 * 4 * 2 * 100 * 4

@@ -45,7 +45,7 @@ def _case(zipage, *, layers, Hkv, d, b, seq_lens, L_max=0, seed=0, heavy=False):
     p = dict(num_layers=layers, num_q_heads=Hkv, num_kv_heads=Hkv, head_dim=d, block_size=b, n_max=mb,
              window=1, alpha=0.5, beta=0.5, decay=0.9, scale=1.0 / np.sqrt(d), protect_window=1, causal=1)
     out = torch.full((R, layers, Hkv, L_row), float("nan"), device="cuda")
-    ws = zipage.new_workspace(zipage.zp_redundancy_workspace_size())
+    ws = zipage.new_workspace(zipage.zp_redundancy_workspace_size(p, R, L_row))
     zipage.zp_redundancy_all_pairs(pool.cuda(), torch.from_numpy(tables).cuda(),
                                    torch.tensor(seq_lens, dtype=torch.int32).cuda(), out, p, ws,
                                    max_seq_len=L_row)
@@ -85,6 +85,6 @@ def test_all_pairs_bad_block_reports(zp):
     pool = torch.zeros((1, 8, 2, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
     tables = torch.tensor([[0, 1, 99, 2]], dtype=torch.int32, device="cuda")
     out = torch.zeros((1, 1, 2, 64), device="cuda")
-    ws = zp.new_workspace(zp.zp_redundancy_workspace_size())
+    ws = zp.new_workspace(zp.zp_redundancy_workspace_size(p, 1))
     zp.zp_redundancy_all_pairs(pool, tables, torch.tensor([50], dtype=torch.int32, device="cuda"), out, p, ws)
     assert zp.zp_read_error(ws) == zp.ZP_ERR_BAD_TABLE
