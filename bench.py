@@ -343,7 +343,7 @@ def run_e2e(args, wl, inp, pristine_pool, pristine_gs, world):
     nl = wl.num_layers
     per = max(1, nl // 16)  # layers per chunk
     chunks = [(c, min(per, nl - c)) for c in range(0, nl, per)]
-    ws = [zipage.new_workspace(zipage.zp_compress_workspace_size(batch.params, inp.num_compress))
+    ws = [zipage.new_workspace(zipage.zp_compress_workspace_size(batch.params, inp.num_compress, batch.max_seq_len))
           for _ in chunks]  # one error word per call
     steps = max(2, min(args.steps, 5))
     bytes_in = (h_pool.numel() * 2 + h_q.numel() * 2 + h_gs.numel() * 4 + 2 * h_tables.numel() * 4

@@ -84,7 +84,7 @@ typedef struct zp_seq_meta {
   const int32_t* qslot;       /* device [R]: query slot of each request, 0 <= qslot < num_qslots */
   const int32_t* dst_tables;  /* device [R][max_blocks]: where survivors go; equals the source
                                  table except at target blocks (zp_plan_compress) */
-  int32_t max_seq_len;        /* L_max: the longest seq_len of the call (<= 4096), or 0 for
+  int32_t max_seq_len;        /* L_max: the longest seq_len of the call (<= 16384), or 0 for
                                  n_max*b.  It is also the row length of global_scores and of
                                  the zp_debug arrays. */
   const int32_t* n_max_per_req; /* device [R] or NULL: per-request block budgets
@@ -143,8 +143,10 @@ zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const
                       const zp_params* params, const zp_debug* dbg, void* workspace,
                       size_t workspace_bytes, zp_stream stream);
 
-/* Bytes of workspace zp_compress needs (the device error word and its padding). */
-size_t zp_compress_workspace_size(const zp_params* params, int32_t num_requests);
+/* Bytes of workspace zp_compress needs: the device error word and unit counter (256 bytes), plus,
+ * when max_seq_len exceeds 4096, the scratch of the multi-pass form (per unit: 1 KB per 256-token
+ * chunk and 16 bytes per token).  max_seq_len 0 means n_max*b. */
+size_t zp_compress_workspace_size(const zp_params* params, int32_t num_requests, int32_t max_seq_len);
 
 /* ---------------------------------------------------------------------------------------
  * Original (all-pairs) redundancy score — the ablation of the Lightning Redundancy Score

@@ -33,47 +33,12 @@
 #include <algorithm>
 #include <mutex>
 
-#include "zp_internal.h"
-#include "zp_ptx.cuh"
+#include "zp_compress_common.cuh"
 
 namespace zp {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kKeysPerCta = 256;
-constexpr int kRows = 128;         // window rows, padded: MMA M of D1 and N of D2
-constexpr int kMaxCluster = 16;    // CTAs per cluster: 8 (portable, 2 CTAs per SM) or 16 (1 per SM)
-constexpr int kMaxEvict = 32;      // E = L - k = b <= 32
-// table entries cached per request for a cluster of up to MAXC CTAs (256 keys each, b >= 16)
-constexpr int max_table(int maxc) { return maxc * (kKeysPerCta / 16); }
-constexpr uint32_t kTmemCols = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 
-struct CompressArgs {
-  uint8_t* pool;
-  int64_t num_blocks;
-  const int32_t* block_tables;
-  const int32_t* dst_tables;
-  const int32_t* seq_len;
-  const int32_t* qslot;
-  const int32_t* n_max_req;         // per-request block budgets, or nullptr
-  float* gscores;
-  int32_t* err;
-  int32_t* work;                    // unit counter of the persistent clusters (zeroed per launch)
-  float* dbg_attn;
-  float* dbg_redund;
-  float* dbg_score;
-  int32_t* dbg_keep;
-  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, max_blocks, num_qslots;  // L: launch length
-  int layer0, nl;                 // the call's layers: [layer0, layer0 + nl) of the `layers`
-  float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
-  float inv_rw;                   // 1 / (w * G_q)
-  uint32_t block_bytes;           // bytes of one (layer, block): 2 * Hkv * b * d * 2
-  uint32_t kv_bytes;              // bytes of the K (or V) part of a block: Hkv * b * d * 2
-  uint32_t row_bytes;             // d * 2
-  int b_shift;                    // log2(b)
-  int protect_window, causal;
-};
 
 template <int MAXC>
 struct __align__(1024) SmemT {
@@ -113,30 +78,6 @@ struct __align__(1024) SmemT {
 static_assert(sizeof(SmemT<8>) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "8-CTA clusters: two CTAs per SM");
 static_assert(sizeof(SmemT<16>) + 1024 <= 227 * 1024, "16-CTA clusters: one CTA per SM");
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Monotone map float -> uint32 (NaN ranks with -inf, -0 with +0).
-__device__ __forceinline__ uint32_t order_bits(float s) {
-  if (s != s) s = -INFINITY;
-  if (s == 0.0f) s = 0.0f;
-  uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Eviction key: smaller = evicted first = lower S, and on equal S the later position.
-__device__ __forceinline__ unsigned long long evict_key(float s, int t) {
-  return (static_cast<unsigned long long>(order_bits(s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(t));
-}
-
 // Sorts one 64-bit key per lane ascending across the warp (bitonic network).
 __device__ __forceinline__ unsigned long long warp_sort32(unsigned long long x, int lane) {
 #pragma unroll
@@ -165,92 +106,6 @@ __device__ __forceinline__ unsigned long long warp_merge_low32(unsigned long lon
     x = ((lane & j) == 0) ? lo : hi;
   }
   return x;
-}
-
-__device__ __forceinline__ void record_error(int32_t* err, int code) {
-  if (err) atomicCAS(err, 0, code);
-}
-
-// Byte offset of row `row` of block `phys`, relative to this unit's head base (layer, K, head).
-__device__ __forceinline__ size_t row_off_bytes(const CompressArgs& a, int phys, int kv, int row) {
-  return static_cast<size_t>(static_cast<uint32_t>(phys)) * a.block_bytes + kv * a.kv_bytes +
-         static_cast<uint32_t>(row) * a.row_bytes;
-}
-
-// Lightning redundancy of the 32 keys [key0, key0 + 32) of one warp (BW = block size 16 or 32),
-// from K in 128-byte-swizzled shared memory, with warp-level mma.sync: the BW x BW Gram of each
-// block (G = K K^T, so one ldmatrix per k-step gives both the A and the B fragments), squared
-// norms from its diagonal, and the in-block row sums of cos(k_t, k_j), j != t, over the tokens
-// the block holds (keys at or past L are excluded).  Returns the redundancy of key key0 + lane.
-template <int BW>
-__device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2][kKeysPerCta * 128], float* inv_n,
-                                                           int key0, int lane, int d, int t0, int L) {
-  constexpr int NT = BW / 8;  // n8 tiles per m16 row tile
-  float acc[2][NT][4];
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
-  for (int ks = 0; ks < (d >> 4); ++ks) {
-    uint32_t f[2][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int row = key0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int chunk = 2 * ks + (lane >> 4);
-      ldmatrix_x4(smem_u32(&K[chunk >> 3][row * 128 + (((chunk & 7) ^ (row & 7)) << 4)]), f[mt]);
-    }
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        // columns 8nt..8nt+7 of the block: rows (sub = nt&1) of m-tile src of the same fragments
-        const int src = (BW == 16) ? mt : (nt >> 1);
-        const int sub = nt & 1;
-        mma_16816_bf16(acc[mt][nt], f[mt], sub ? f[src][1] : f[src][0], sub ? f[src][3] : f[src][2]);
-      }
-  }
-  const int g = lane >> 2, tq = lane & 3;
-  // squared norms from the diagonal -> reciprocal norms in shared memory
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = 16 * mt + g + 8 * (e >> 1);
-        const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + (e & 1);
-        if (row == col) inv_n[key0 + row] = 1.0f / fmaxf(sqrtf(fmaxf(acc[mt][nt][e], 0.0f)), 1e-12f);
-      }
-  __syncwarp();
-  float rr[2][2];  // redundancy of rows 16mt + 8hf + g
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int row = 16 * mt + 8 * hf + g;
-      float sum = 0.0f;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + e;
-          const bool ok = col != row && t0 + key0 + col < L;
-          sum += ok ? acc[mt][nt][2 * hf + e] * inv_n[key0 + col] : 0.0f;
-        }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      const int bstart = (BW == 16) ? 16 * mt : 0;             // block of this row within the warp
-      const int m = min(BW, L - (t0 + key0 + bstart));         // tokens the block holds
-      rr[mt][hf] = m > 1 ? sum * inv_n[key0 + row] / static_cast<float>(m - 1) : 0.0f;
-    }
-  // deliver: lane k takes row k, computed by lane 4 * (k % 8)
-  const int srcl = 4 * (lane & 7);
-  const float v00 = __shfl_sync(0xffffffffu, rr[0][0], srcl), v01 = __shfl_sync(0xffffffffu, rr[0][1], srcl);
-  const float v10 = __shfl_sync(0xffffffffu, rr[1][0], srcl), v11 = __shfl_sync(0xffffffffu, rr[1][1], srcl);
-  const int mt = lane >> 4, hf = (lane >> 3) & 1;
-  return mt ? (hf ? v11 : v10) : (hf ? v01 : v00);
 }
 
 template <int MAXC>
@@ -870,7 +725,15 @@ zp_status launch_compress(const CUtensorMap& tmK, const CUtensorMap& tmQ, const 
 
 using namespace zp;
 
-extern "C" size_t zp_compress_workspace_size(const zp_params*, int32_t) { return 256; }  // error word + unit counter
+// The error word and the unit counter; sequences beyond one cluster (L > 4096) add the
+// scratch of the multi-pass form.
+extern "C" size_t zp_compress_workspace_size(const zp_params* p, int32_t num_requests, int32_t max_seq_len) {
+  if (!p || num_requests < 0) return 0;
+  const int64_t L = max_seq_len > 0 ? max_seq_len : static_cast<int64_t>(p->n_max) * p->block_size;
+  if (L <= static_cast<int64_t>(kMaxCluster) * kKeysPerCta) return 256;
+  return 256 + compress_long_scratch_bytes(static_cast<int64_t>(num_requests) * p->num_layers * p->num_kv_heads,
+                                           static_cast<int>(L));
+}
 
 extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
                                  const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
@@ -881,7 +744,8 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   // with no request the per-request arrays may be empty (NULL)
   if (meta->num_requests > 0 && (!block_tables || !meta->seq_len || !meta->qslot || !meta->dst_tables))
     return ZP_ERR_INVALID_ARG;
-  if (workspace_bytes < zp_compress_workspace_size(p, meta->num_requests) || !aligned(workspace, 256))
+  if (workspace_bytes < zp_compress_workspace_size(p, meta->num_requests, meta->max_seq_len) ||
+      !aligned(workspace, 256))
     return ZP_ERR_INVALID_ARG;
   const int layers = p->num_layers, Hq = p->num_q_heads, Hkv = p->num_kv_heads, d = p->head_dim,
             b = p->block_size, n_max = p->n_max, w = p->window, R = meta->num_requests;
@@ -900,8 +764,10 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   if (meta->max_blocks < (L + b - 1) / b) return ZP_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ZP_ERR_UNSUPPORTED;
   if (b != 16 && b != 32) return ZP_ERR_UNSUPPORTED;
-  if (Rw > kRows || n_max > max_table(kMaxCluster) || (L + kKeysPerCta - 1) / kKeysPerCta > kMaxCluster)
-    return ZP_ERR_UNSUPPORTED;
+  // one cluster of up to 16 CTAs covers L <= 4096; longer sequences (to 16384) take the
+  // multi-pass form
+  // (n_max <= L/b + 1 <= max_table(16) whenever one cluster covers L)
+  if (Rw > kRows || L > 16384) return ZP_ERR_UNSUPPORTED;
   if (Gq > 256 || w > 256) return ZP_ERR_UNSUPPORTED;
   if (!aligned(pool->base, 16) || !aligned(obs_q, 16)) return ZP_ERR_INVALID_ARG;
   if (static_cast<int64_t>(layers) * pool->num_blocks >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
@@ -970,6 +836,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.causal = p->causal;
 
   const int C = (L + kKeysPerCta - 1) / kKeysPerCta;
+  if (C > kMaxCluster) return launch_compress_long(tmK, tmQ, a, static_cast<uint8_t*>(workspace) + 256, st);
   const int64_t num_units = static_cast<int64_t>(R) * nl * Hkv;
   return C <= 8 ? launch_compress<8>(tmK, tmQ, a, C, num_units, st) : launch_compress<16>(tmK, tmQ, a, C, num_units, st);
 }

@@ -1,0 +1,166 @@
+// zp_compress_common.cuh — definitions shared by the fused compression pass (zp_compress.cu)
+// and its multi-pass form for sequences longer than one cluster (zp_compress_long.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "zp_internal.h"
+#include "zp_ptx.cuh"
+
+namespace zp {
+
+constexpr int kThreads = 256;
+constexpr int kKeysPerCta = 256;
+constexpr int kRows = 128;         // window rows, padded: MMA M of D1 and N of D2
+constexpr int kMaxCluster = 16;    // CTAs per cluster: 8 (portable, 2 CTAs per SM) or 16 (1 per SM)
+constexpr int kMaxEvict = 32;      // E = L - k = b <= 32
+// table entries cached per request for a cluster of up to MAXC CTAs (256 keys each, b >= 16)
+constexpr int max_table(int maxc) { return maxc * (kKeysPerCta / 16); }
+constexpr uint32_t kTmemCols = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+
+struct CompressArgs {
+  uint8_t* pool;
+  int64_t num_blocks;
+  const int32_t* block_tables;
+  const int32_t* dst_tables;
+  const int32_t* seq_len;
+  const int32_t* qslot;
+  const int32_t* n_max_req;         // per-request block budgets, or nullptr
+  float* gscores;
+  int32_t* err;
+  int32_t* work;                    // unit counter of the persistent clusters (zeroed per launch)
+  float* dbg_attn;
+  float* dbg_redund;
+  float* dbg_score;
+  int32_t* dbg_keep;
+  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, max_blocks, num_qslots;  // L: launch length
+  int layer0, nl;                 // the call's layers: [layer0, layer0 + nl) of the `layers`
+  float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
+  float inv_rw;                   // 1 / (w * G_q)
+  uint32_t block_bytes;           // bytes of one (layer, block): 2 * Hkv * b * d * 2
+  uint32_t kv_bytes;              // bytes of the K (or V) part of a block: Hkv * b * d * 2
+  uint32_t row_bytes;             // d * 2
+  int b_shift;                    // log2(b)
+  int protect_window, causal;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Monotone map float -> uint32 (NaN ranks with -inf, -0 with +0).
+__device__ __forceinline__ uint32_t order_bits(float s) {
+  if (s != s) s = -INFINITY;
+  if (s == 0.0f) s = 0.0f;
+  uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Eviction key: smaller = evicted first = lower S, and on equal S the later position.
+__device__ __forceinline__ unsigned long long evict_key(float s, int t) {
+  return (static_cast<unsigned long long>(order_bits(s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(t));
+}
+
+__device__ __forceinline__ void record_error(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Byte offset of row `row` of block `phys`, relative to this unit's head base (layer, K, head).
+__device__ __forceinline__ size_t row_off_bytes(const CompressArgs& a, int phys, int kv, int row) {
+  return static_cast<size_t>(static_cast<uint32_t>(phys)) * a.block_bytes + kv * a.kv_bytes +
+         static_cast<uint32_t>(row) * a.row_bytes;
+}
+
+// Lightning redundancy of the 32 keys [key0, key0 + 32) of one warp (BW = block size 16 or 32),
+// from K in 128-byte-swizzled shared memory, with warp-level mma.sync: the BW x BW Gram of each
+// block (G = K K^T, so one ldmatrix per k-step gives both the A and the B fragments), squared
+// norms from its diagonal, and the in-block row sums of cos(k_t, k_j), j != t, over the tokens
+// the block holds (keys at or past L are excluded).  Returns the redundancy of key key0 + lane.
+template <int BW>
+__device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2][kKeysPerCta * 128], float* inv_n,
+                                                           int key0, int lane, int d, int t0, int L) {
+  constexpr int NT = BW / 8;  // n8 tiles per m16 row tile
+  float acc[2][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
+  for (int ks = 0; ks < (d >> 4); ++ks) {
+    uint32_t f[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int row = key0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int chunk = 2 * ks + (lane >> 4);
+      ldmatrix_x4(smem_u32(&K[chunk >> 3][row * 128 + (((chunk & 7) ^ (row & 7)) << 4)]), f[mt]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        // columns 8nt..8nt+7 of the block: rows (sub = nt&1) of m-tile src of the same fragments
+        const int src = (BW == 16) ? mt : (nt >> 1);
+        const int sub = nt & 1;
+        mma_16816_bf16(acc[mt][nt], f[mt], sub ? f[src][1] : f[src][0], sub ? f[src][3] : f[src][2]);
+      }
+  }
+  const int g = lane >> 2, tq = lane & 3;
+  // squared norms from the diagonal -> reciprocal norms in shared memory
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = 16 * mt + g + 8 * (e >> 1);
+        const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + (e & 1);
+        if (row == col) inv_n[key0 + row] = 1.0f / fmaxf(sqrtf(fmaxf(acc[mt][nt][e], 0.0f)), 1e-12f);
+      }
+  __syncwarp();
+  float rr[2][2];  // redundancy of rows 16mt + 8hf + g
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int row = 16 * mt + 8 * hf + g;
+      float sum = 0.0f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + e;
+          const bool ok = col != row && t0 + key0 + col < L;
+          sum += ok ? acc[mt][nt][2 * hf + e] * inv_n[key0 + col] : 0.0f;
+        }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      const int bstart = (BW == 16) ? 16 * mt : 0;             // block of this row within the warp
+      const int m = min(BW, L - (t0 + key0 + bstart));         // tokens the block holds
+      rr[mt][hf] = m > 1 ? sum * inv_n[key0 + row] / static_cast<float>(m - 1) : 0.0f;
+    }
+  // deliver: lane k takes row k, computed by lane 4 * (k % 8)
+  const int srcl = 4 * (lane & 7);
+  const float v00 = __shfl_sync(0xffffffffu, rr[0][0], srcl), v01 = __shfl_sync(0xffffffffu, rr[0][1], srcl);
+  const float v10 = __shfl_sync(0xffffffffu, rr[1][0], srcl), v11 = __shfl_sync(0xffffffffu, rr[1][1], srcl);
+  const int mt = lane >> 4, hf = (lane >> 3) & 1;
+  return mt ? (hf ? v11 : v10) : (hf ? v01 : v00);
+}
+
+
+// Multi-pass compression of sequences longer than one cluster (L > 4096), in
+// zp_compress_long.cu.  `scratch` is the workspace past its first 256 bytes.
+size_t compress_long_scratch_bytes(int64_t units, int L);
+zp_status launch_compress_long(const CUtensorMap& tmK, const CUtensorMap& tmQ, const CompressArgs& a,
+                               void* scratch, cudaStream_t st);
+
+}  // namespace zp

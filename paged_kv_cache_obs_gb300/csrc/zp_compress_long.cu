@@ -1,0 +1,506 @@
+// zp_compress_long.cu — the compression pass in several launches, for sequences longer than
+// one thread-block cluster covers (4096 < L <= 16384 tokens: the first compression after a very
+// long prompt, zh §2.1).  Same operation, readings and results as the fused pass
+// (zp_compress.cu), with the cluster's exchanges replaced by kernel boundaries and global
+// scratch (the workspace past its first 256 bytes):
+//   1. stats:   per (unit, 256-key chunk): TMA of K and Q, tcgen05 D1 = Q K^T into TMEM, each
+//               window row's (max, exp-sum) over the chunk's visible keys, and the Lightning
+//               redundancy of the chunk's keys (warp-level MMA);
+//   2. score:   per (unit, chunk): every row's normaliser from all chunks' partials, K and Q
+//               again, D2 = K Q^T, the attention mass of each key and S = attn + a*G - b*R;
+//   3. select:  per unit: the E = L - k lowest eviction keys by an 8-pass radix select of the
+//               64-bit keys (order(S), ~t), destinations by a block-wide scan, and the global
+//               scores updated in place (every read before any write);
+//   4. compact: per unit: the moved K and V rows, 128 source rows at a time in increasing
+//               order (dst <= src, so a chunk's rows are read before anything lands on them).
+// Every wait is bounded.  A unit with bad metadata or block ids is reported and left untouched.
+#include <algorithm>
+#include <mutex>
+
+#include "zp_compress_common.cuh"
+
+namespace zp {
+namespace {
+
+constexpr int kMaxLongL = 16384;
+constexpr int kSelThreads = 1024;
+constexpr int kCompactRows = 128;
+
+struct LongScratch {
+  float2* part;  // [units][nch][kRows] (max, exp-sum) of each window row over each chunk
+  float* attn;   // [units][L]
+  float* red;    // [units][L]
+  float* score;  // [units][L]
+  int32_t* dst;  // [units][L]: destination slot of each kept key, -1 if evicted
+  int nch;       // 256-key chunks per unit at the launch length
+};
+
+struct __align__(1024) LongSmem {
+  uint8_t K[2][kKeysPerCta * 128];  // [d-half][row][128 B], 128-byte swizzle
+  uint8_t Q[2][kRows * 128];
+  float2 part[2][kRows];
+  float row_off[kRows];
+  float inv_n[kKeysPerCta];
+  uint64_t bar_tma, bar_mma;
+  uint32_t tmem_base;
+};
+
+struct UnitMeta {
+  int r, layer, h, L, n_max_r, k_r, slot;
+  bool bad;
+};
+
+__device__ __forceinline__ UnitMeta unit_meta(const CompressArgs& a, int unit) {
+  UnitMeta m;
+  m.h = unit % a.Hkv;
+  m.r = unit / a.Hkv / a.nl;
+  m.layer = a.layer0 + (unit / a.Hkv) % a.nl;
+  m.L = a.seq_len[m.r];
+  m.n_max_r = a.n_max_req ? a.n_max_req[m.r] : a.n_max;
+  m.k_r = (m.n_max_r - 1) * a.b;
+  m.slot = a.qslot[m.r];
+  m.bad = (m.n_max_r < 2) || (m.n_max_r > a.n_max) || (m.k_r < a.w) || (m.L <= m.k_r) || (m.L > a.L) ||
+          m.slot < 0 || m.slot >= a.num_qslots;
+  return m;
+}
+
+// TMA of the chunk's K blocks and the unit's window queries, D1 or D2 on tcgen05, shared by the
+// stats and score kernels.  Returns false if a bounded wait gave up.  (tid 0)
+__device__ __forceinline__ bool load_kq(LongSmem& s, const CUtensorMap* tmK, const CUtensorMap* tmQ,
+                                        const CompressArgs& a, const UnitMeta& m, const int* phys, int nblk,
+                                        uint32_t& ph_tma) {
+  const int nhalf = a.d / 64;
+  mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>(((nblk << a.b_shift) + a.Rw) * a.d * 2));
+  for (int hd = 0; hd < nhalf; ++hd)
+    tma_load_3d(&s.Q[hd][0], tmQ, &s.bar_tma, hd * 64, m.h * a.Gq, (m.slot * a.layers + m.layer) * a.w);
+  for (int bi = 0; bi < nblk; ++bi)
+    for (int hd = 0; hd < nhalf; ++hd)
+      tma_load_3d(&s.K[hd][bi * a.b * 128], tmK, &s.bar_tma, hd * 64, m.h * a.b,
+                  m.layer * static_cast<int>(a.num_blocks) + phys[bi]);
+  const bool ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
+  if (ok) ph_tma ^= 1;
+  return ok;
+}
+
+// Common prologue of the stats and score kernels: the chunk's block ids (checked), mbarriers,
+// TMEM, zeroed Q padding rows.  Returns the number of blocks, or -1 if the chunk has no work.
+__device__ __forceinline__ int chunk_prologue(LongSmem& s, const CompressArgs& a, const UnitMeta& m, int t0,
+                                              int* phys, int tid) {
+  const int nk = max(0, min(kKeysPerCta, m.L - t0));
+  if (m.bad || nk == 0) return -1;  // uniform over the CTA
+  const int nblk = (nk + a.b - 1) >> a.b_shift;
+  __shared__ int bad_blk;
+  if (tid == 0) bad_blk = 0;
+  __syncthreads();
+  if (tid < nblk) {
+    const int p = a.block_tables[static_cast<int64_t>(m.r) * a.max_blocks + (t0 >> a.b_shift) + tid];
+    phys[tid] = p;
+    if (p < 0 || p >= a.num_blocks) bad_blk = 1;
+  }
+  if (tid == 0) {
+    mbar_init(&s.bar_tma, 1);
+    mbar_init(&s.bar_mma, 1);
+    fence_mbar_init();
+  }
+  for (int i = a.Rw * 8 + tid; i < kRows * 8; i += kThreads) {  // padding rows of Q are zero
+    reinterpret_cast<uint4*>(s.Q[0])[i] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(s.Q[1])[i] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (bad_blk) return -1;  // reported by the select kernel
+  return nblk;
+}
+
+// 1. Row statistics over the chunk and Lightning redundancy of its keys.
+__global__ void __launch_bounds__(kThreads, 2)
+    long_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                      const CompressArgs a, const LongScratch sc) {
+  extern __shared__ uint8_t smem_raw[];
+  LongSmem& s = *reinterpret_cast<LongSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ int phys[kKeysPerCta / 16];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, hh = warp >> 2;
+  const int unit = static_cast<int>(blockIdx.x) / sc.nch, ch = static_cast<int>(blockIdx.x) % sc.nch;
+  const int t0 = ch * kKeysPerCta;
+  const UnitMeta m = unit_meta(a, unit);
+  float2* part = sc.part + (static_cast<int64_t>(unit) * sc.nch + ch) * kRows;
+  const int nblk = chunk_prologue(s, a, m, t0, phys, tid);
+  if (nblk < 0) {
+    if (tid < kRows) part[tid] = make_float2(-INFINITY, 0.0f);
+    return;
+  }
+  const int nk = min(kKeysPerCta, m.L - t0);
+  if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  bool ok = true;
+  uint32_t ph_tma = 0;
+  if (tid == 0) {
+    ok = load_kq(s, &tmK, &tmQ, a, m, phys, nblk, ph_tma);
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16_f32(128, (nk + 15) & ~15);
+    for (int kk = 0; kk < a.d / 16; ++kk)
+      mma_bf16(tbase, smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32])),
+               smem_desc_sw128(smem_u32(&s.K[kk >> 2][(kk & 3) * 32])), idesc, kk > 0);
+    mma_commit(&s.bar_mma);
+    ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
+  }
+  const bool fail = __syncthreads_or(!ok);
+  tc_fence_after();
+  if (!fail) {
+    // thread = window row i, warp half hh = 128 key columns; keys t <= L-w+i/G_q are visible
+    const int i = q4 * 32 + lane;
+    const int cbase = hh * 128, ncol = nk - cbase;
+    const int vlim = max(0, min(ncol, (a.causal ? (m.L - a.w + i / a.Gq) : (m.L - 1)) - t0 - cbase + 1));
+    const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
+    float mx = -INFINITY, ls = 0.0f;
+    for (int c2 = 0; c2 < 4 && c2 * 32 < ncol; ++c2) {
+      float v[32];
+      tmem_ld32(tl + c2 * 32, v);
+      float cm = mx;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c2 * 32 + j < vlim) cm = fmaxf(cm, v[j]);
+      if (cm == -INFINITY) continue;
+      if (mx != -INFINITY && cm > mx) ls *= ex2((mx - cm) * a.sl2);
+      mx = cm;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c2 * 32 + j < vlim) ls += ex2(fmaf(v[j], a.sl2, -mx * a.sl2));
+    }
+    s.part[hh][i] = make_float2(mx, ls);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (!fail && tid < kRows) {
+    const float2 p0 = s.part[0][tid], p1 = s.part[1][tid];
+    float mm = fmaxf(p0.x, p1.x), l = 0.0f;
+    if (tid >= a.Rw) mm = -INFINITY;  // a padding row of the MMA, not a window row
+    if (mm != -INFINITY) {
+      if (p0.y > 0.0f) l += p0.y * ex2((p0.x - mm) * a.sl2);
+      if (p1.y > 0.0f) l += p1.y * ex2((p1.x - mm) * a.sl2);
+    }
+    part[tid] = make_float2(mm, l);
+  } else if (fail && tid < kRows) {
+    part[tid] = make_float2(-INFINITY, 0.0f);
+  }
+  if (fail && tid == 0) record_error(a.err, ZP_ERR_TIMEOUT);
+  if (!fail && warp * 32 < nk) {
+    const float red = (a.b == 16) ? warp_lightning_redundancy<16>(s.K, s.inv_n, warp * 32, lane, a.d, t0, m.L)
+                                  : warp_lightning_redundancy<32>(s.K, s.inv_n, warp * 32, lane, a.d, t0, m.L);
+    if (tid < nk) {
+      const int64_t o = static_cast<int64_t>(unit) * a.L + t0 + tid;
+      sc.red[o] = red;
+      if (a.dbg_redund) a.dbg_redund[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t0 + tid] = red;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+// 2. Attention mass of each key (every row normalised over all chunks) and its score S.
+__global__ void __launch_bounds__(kThreads, 2)
+    long_score_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                      const CompressArgs a, const LongScratch sc) {
+  extern __shared__ uint8_t smem_raw[];
+  LongSmem& s = *reinterpret_cast<LongSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ int phys[kKeysPerCta / 16];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int q4 = warp & 3, hh = warp >> 2;
+  const int unit = static_cast<int>(blockIdx.x) / sc.nch, ch = static_cast<int>(blockIdx.x) % sc.nch;
+  const int t0 = ch * kKeysPerCta;
+  const UnitMeta m = unit_meta(a, unit);
+  const int nblk = chunk_prologue(s, a, m, t0, phys, tid);
+  if (nblk < 0) return;
+  const int nk = min(kKeysPerCta, m.L - t0);
+  // every row's normaliser: log2 of its exp-sum over all chunks, relative to its max
+  if (tid < kRows) {
+    const float2* pu = sc.part + static_cast<int64_t>(unit) * sc.nch * kRows;
+    const int nc = (m.L + kKeysPerCta - 1) / kKeysPerCta;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, pu[c * kRows + tid].x);
+    float Z = 0.0f;
+    if (M != -INFINITY)
+      for (int c = 0; c < nc; ++c) {
+        const float2 p = pu[c * kRows + tid];
+        if (p.y > 0.0f) Z += p.y * ex2((p.x - M) * a.sl2);
+      }
+    s.row_off[tid] = (tid < a.Rw && Z > 0.0f) ? fmaf(M, a.sl2, lg2(Z)) : INFINITY;
+  }
+  if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  bool ok = true;
+  uint32_t ph_tma = 0;
+  if (tid == 0) {
+    ok = load_kq(s, &tmK, &tmQ, a, m, phys, nblk, ph_tma);
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16_f32(128, 128);
+    for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
+      for (int kk = 0; kk < a.d / 16; ++kk)
+        mma_bf16(tbase + kh * 128, smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32])),
+                 smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32])), idesc, kk > 0);
+    mma_commit(&s.bar_mma);
+    ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
+  }
+  const bool fail = __syncthreads_or(!ok);
+  tc_fence_after();
+  const int kt = t0 + tid;
+  const int wcol = hh * 128 + q4 * 32;
+  float attn = 0.0f;
+  if (!fail && wcol < nk) {
+    // thread = key (TMEM lane), columns = window rows; row i sees key kt iff kt <= L-w+i/G_q
+    const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128;
+    const int imin = a.causal ? max(0, a.Gq * (kt - (m.L - a.w))) : 0;
+    float acc = 0.0f;
+    for (int c2 = 0; c2 < 4 && c2 * 32 < a.Rw; ++c2) {
+      float v[32];
+      tmem_ld32(tl + c2 * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int row = c2 * 32 + j;
+        const float p = ex2(fmaf(v[j], a.sl2, -s.row_off[row]));
+        if (row >= imin) acc += p;
+      }
+    }
+    attn = acc * a.inv_rw;
+  }
+  if (!fail && tid < nk) {
+    const float g = a.gscores[((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L + kt];
+    const int64_t o = static_cast<int64_t>(unit) * a.L + kt;
+    float S = (attn + a.alpha * g) - a.beta * sc.red[o];
+    if (a.protect_window && kt >= m.L - a.w) S = INFINITY;
+    sc.attn[o] = attn;
+    sc.score[o] = S;
+    const int64_t od = ((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + kt;
+    if (a.dbg_attn) a.dbg_attn[od] = attn;
+    if (a.dbg_score) a.dbg_score[od] = S;
+  }
+  if (fail && tid == 0) record_error(a.err, ZP_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+// 3. Selection, destinations and the global-score update, one CTA per unit.
+__global__ void __launch_bounds__(kSelThreads) long_select_kernel(const CompressArgs a, const LongScratch sc) {
+  constexpr int kPer = kMaxLongL / kSelThreads;  // keys per thread (contiguous positions)
+  __shared__ unsigned hist[256];
+  __shared__ unsigned long long sh_prefix;
+  __shared__ unsigned sh_rank;
+  __shared__ int warp_sum[kSelThreads / 32];
+  __shared__ int bad_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.x;
+  const UnitMeta m = unit_meta(a, unit);
+  int32_t* dst = sc.dst + static_cast<int64_t>(unit) * a.L;
+  if (tid == 0) bad_s = m.bad ? 1 : 0;
+  __syncthreads();
+  if (!m.bad) {  // every block id the unit reads or writes
+    const int nsrc = (m.L + a.b - 1) >> a.b_shift;
+    for (int i = tid; i < nsrc; i += kSelThreads) {
+      const int p = a.block_tables[static_cast<int64_t>(m.r) * a.max_blocks + i];
+      if (p < 0 || p >= a.num_blocks) bad_s = 1;
+    }
+    for (int i = tid; i < m.n_max_r - 1; i += kSelThreads) {
+      const int p = a.dst_tables[static_cast<int64_t>(m.r) * a.max_blocks + i];
+      if (p < 0 || p >= a.num_blocks) bad_s = 1;
+    }
+  }
+  __syncthreads();
+  if (bad_s) {  // reported; the unit keeps its pool rows and global scores
+    if (tid == 0) record_error(a.err, ZP_ERR_BAD_TABLE);
+    for (int t = tid; t < a.L; t += kSelThreads) dst[t] = -1;
+    return;
+  }
+  const int L = m.L, E = L - m.k_r;
+  const float* S = sc.score + static_cast<int64_t>(unit) * a.L;
+  const int p0 = tid * kPer;  // this thread's positions [p0, p0 + kPer)
+  // radix select of the E-th smallest key, 8 bits at a time from the top
+  unsigned long long prefix = 0, mask = 0;
+  unsigned rank = static_cast<unsigned>(E);
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    for (int e = 0; e < kPer; ++e) {
+      const int t = p0 + e;
+      if (t >= L) break;
+      const unsigned long long key = evict_key(S[t], t);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFF], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // the bucket holding the rank-th key: inclusive prefix sums of 8 bins per lane
+      unsigned c[8], run = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        run += hist[lane * 8 + q];
+        c[q] = run;
+      }
+      unsigned incl = run;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const unsigned before = incl - run;  // keys in the lanes below
+      if (before < rank && rank <= incl) {
+        int q = 0;
+        while (before + c[q] < rank) ++q;
+        sh_prefix = prefix | (static_cast<unsigned long long>(lane * 8 + q) << shift);
+        sh_rank = rank - (before + (q ? c[q - 1] : 0u));
+      }
+    }
+    __syncthreads();
+    prefix = sh_prefix;
+    rank = sh_rank;
+    mask |= 0xFFull << shift;
+  }
+  const unsigned long long T = prefix;  // exactly E keys are <= T (keys are distinct)
+  // destinations: j = number of kept keys before t
+  int kept_here = 0;
+  for (int e = 0; e < kPer; ++e) {
+    const int t = p0 + e;
+    if (t < L && evict_key(S[t], t) > T) ++kept_here;
+  }
+  int incl = kept_here;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int before = incl - kept_here;
+  for (int w2 = 0; w2 < warp; ++w2) before += warp_sum[w2];
+  // global scores: every read of the unit's row before any write of it
+  float* G = a.gscores + ((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
+  const float* attn = sc.attn + static_cast<int64_t>(unit) * a.L;
+  float gnew[kPer];
+  int jdst[kPer];
+  int j = before;
+  for (int e = 0; e < kPer; ++e) {
+    const int t = p0 + e;
+    jdst[e] = -1;
+    gnew[e] = 0.0f;
+    if (t >= L) continue;
+    if (evict_key(S[t], t) > T) {
+      jdst[e] = j++;
+      gnew[e] = a.decay * G[t] + attn[t];
+    }
+  }
+  __syncthreads();
+  for (int e = 0; e < kPer; ++e) {
+    const int t = p0 + e;
+    if (t >= a.L) break;
+    dst[t] = jdst[e];
+    if (t >= L) continue;
+    if (jdst[e] >= 0) G[jdst[e]] = gnew[e];
+    if (a.dbg_keep) a.dbg_keep[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t] = jdst[e] >= 0;
+  }
+  __syncthreads();
+  for (int t = m.k_r + tid; t < L; t += kSelThreads) G[t] = 0.0f;  // slots past the k survivors
+}
+
+// 4. In-place compaction of the moved K and V rows, one CTA per unit, 128 source rows at a time.
+__global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressArgs a, const LongScratch sc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint4* stage = reinterpret_cast<uint4*>(smem_raw);  // [kCompactRows][2 * d / 8] 16-byte pieces
+  __shared__ int moved_dst[kCompactRows];
+  const int tid = threadIdx.x;
+  const int unit = blockIdx.x;
+  const UnitMeta m = unit_meta(a, unit);
+  if (m.bad) return;
+  const int32_t* dst = sc.dst + static_cast<int64_t>(unit) * a.L;
+  const int32_t* src_tab = a.block_tables + static_cast<int64_t>(m.r) * a.max_blocks;
+  const int32_t* dst_tab = a.dst_tables + static_cast<int64_t>(m.r) * a.max_blocks;
+  uint8_t* const head_base = a.pool + static_cast<size_t>(m.layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
+                             static_cast<size_t>(m.h) * a.b * a.row_bytes;
+  const int bm = a.b - 1, pieces = 2 * a.d / 8;  // 16-byte pieces of a row's K and V
+  for (int c0 = 0; c0 < m.L; c0 += kCompactRows) {
+    if (tid < kCompactRows) {
+      const int t = c0 + tid;
+      int md = -1;
+      if (t < m.L) {
+        const int jj = dst[t];  // -1 for an evicted key (or a reported unit)
+        if (jj >= 0 && (src_tab[t >> a.b_shift] != dst_tab[jj >> a.b_shift] || (t & bm) != (jj & bm))) md = jj;
+      }
+      moved_dst[tid] = md;
+    }
+    __syncthreads();
+    for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
+      const int row = i / pieces, pc = i % pieces, t = c0 + row;
+      if (moved_dst[row] < 0) continue;
+      const int kv = pc >= pieces / 2, off = (pc % (pieces / 2)) * 16;
+      stage[i] = *reinterpret_cast<const uint4*>(
+          head_base + static_cast<size_t>(static_cast<uint32_t>(src_tab[t >> a.b_shift])) * a.block_bytes +
+          kv * a.kv_bytes + static_cast<uint32_t>(t & bm) * a.row_bytes + off);
+    }
+    __syncthreads();  // every read of the chunk precedes every write landing on it
+    for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
+      const int row = i / pieces, pc = i % pieces;
+      const int jj = moved_dst[row];
+      if (jj < 0) continue;
+      const int kv = pc >= pieces / 2, off = (pc % (pieces / 2)) * 16;
+      *reinterpret_cast<uint4*>(head_base + static_cast<size_t>(static_cast<uint32_t>(dst_tab[jj >> a.b_shift])) * a.block_bytes +
+                                kv * a.kv_bytes + static_cast<uint32_t>(jj & bm) * a.row_bytes + off) = stage[i];
+    }
+    __syncthreads();
+  }
+}
+
+static_assert(sizeof(LongSmem) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "two CTAs per SM");
+
+}  // namespace
+
+size_t compress_long_scratch_bytes(int64_t units, int L) {
+  const int64_t nch = (L + kKeysPerCta - 1) / kKeysPerCta;
+  return static_cast<size_t>(units) * (static_cast<size_t>(nch) * kRows * sizeof(float2) + static_cast<size_t>(L) * 16);
+}
+
+zp_status launch_compress_long(const CUtensorMap& tmK, const CUtensorMap& tmQ, const CompressArgs& a, void* scratch,
+                               cudaStream_t st) {
+  if (a.L > kMaxLongL) return ZP_ERR_UNSUPPORTED;
+  const int64_t units = static_cast<int64_t>(a.R) * a.nl * a.Hkv;
+  LongScratch sc{};
+  sc.nch = (a.L + kKeysPerCta - 1) / kKeysPerCta;
+  uint8_t* p = static_cast<uint8_t*>(scratch);
+  sc.part = reinterpret_cast<float2*>(p);
+  p += static_cast<size_t>(units) * sc.nch * kRows * sizeof(float2);
+  sc.attn = reinterpret_cast<float*>(p);
+  p += static_cast<size_t>(units) * a.L * 4;
+  sc.red = reinterpret_cast<float*>(p);
+  p += static_cast<size_t>(units) * a.L * 4;
+  sc.score = reinterpret_cast<float*>(p);
+  p += static_cast<size_t>(units) * a.L * 4;
+  sc.dst = reinterpret_cast<int32_t*>(p);
+  if (units * sc.nch >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(LongSmem) + 1024;
+  const size_t cmp_smem = static_cast<size_t>(kCompactRows) * 2 * a.d * 2;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(long_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(long_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(long_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kCompactRows * 2 * 128 * 2);
+  });
+  if (attr != cudaSuccess) return ZP_ERR_CUDA;
+  const unsigned chunks = static_cast<unsigned>(units * sc.nch);
+  long_stats_kernel<<<chunks, kThreads, smem, st>>>(tmK, tmQ, a, sc);
+  long_score_kernel<<<chunks, kThreads, smem, st>>>(tmK, tmQ, a, sc);
+  long_select_kernel<<<static_cast<unsigned>(units), kSelThreads, 0, st>>>(a, sc);
+  long_compact_kernel<<<static_cast<unsigned>(units), kThreads, cmp_smem, st>>>(a, sc);
+  return cudaGetLastError() == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
+}
+
+}  // namespace zp

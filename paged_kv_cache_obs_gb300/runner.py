@@ -41,14 +41,15 @@ class CompressionBatch:
         self.d_qslot = torch.from_numpy(inp.qslot).to(dev)
         self.obs_q = inp.obs_q.to(dev)
         self.gs = inp.global_scores.to(dev)
-        self.workspace = zipage.new_workspace(zipage.zp_compress_workspace_size(self.params, R), dev)
-        self.d_nmax = None if self.n_max_req is None else torch.from_numpy(self.n_max_req).to(dev)
-        self.debug = None
         # the row length of the global scores is the longest sequence the call may hold (more
         # than n_max*b only when requests left a long prefill)
         self.seq_len = np.ascontiguousarray(inp.seq_len[:R])
         row = inp.global_scores.shape[-1]
         self.max_seq_len = row if row != wl.L else 0
+        self.workspace = zipage.new_workspace(
+            zipage.zp_compress_workspace_size(self.params, R, self.max_seq_len), dev)
+        self.d_nmax = None if self.n_max_req is None else torch.from_numpy(self.n_max_req).to(dev)
+        self.debug = None
 
     def enable_debug(self):
         R, nl, Hkv = self.inp.num_compress, self.wl.num_layers, self.wl.num_kv_heads

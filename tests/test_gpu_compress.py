@@ -90,6 +90,12 @@ SMALL = {
                                                         num_q_heads=8, n_max=200),
     "long_prefill": synth.WORKLOADS["prefill"].scaled(num_requests=6, num_layers=1, num_kv_heads=2,
                                                       num_q_heads=8, n_max=64, prefill_max=4000),
+    # beyond one cluster: the multi-pass form (launch length above 4096).  Long prefills up to
+    # 9000 tokens (E up to about 8000), and a decode trigger at L = 4800 (N_max = 300, E = 16)
+    "multipass_prefill": synth.WORKLOADS["prefill"].scaled(num_requests=4, num_layers=1, num_kv_heads=2,
+                                                           num_q_heads=8, n_max=64, prefill_max=9000),
+    "multipass_trigger": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
+                                                             num_q_heads=8, n_max=300),
 }
 
 
