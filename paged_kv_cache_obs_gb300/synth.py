@@ -19,6 +19,8 @@ Workloads (sizes as in the workload list of this project):
                U{1..16} tokens
   prefill      llama3_8b shape with N_max 64 (k = 1008): 64 requests that left a long prefill and
                hold U{1009..2048} tokens each (first compression after the prompt); G ~ U(0,1)
+  prefill_long llama3_8b shape with N_max 128 (k = 2032): 16 requests holding U{2033..8192}
+               tokens each (prompts beyond one cluster: the multi-pass form)
 Physical block ids are a seeded random permutation over the pool in every workload.
 Seeds: 0x5A1F0000 + workload index.
 """
@@ -87,6 +89,9 @@ WORKLOADS = {
                       num_decode=224),
     "prefill": Workload("prefill", 5, 64, 32, 32, 8, 128, 16, 64, 32, key_recipe="clustered",
                         prefill_max=2048),
+    # prompts beyond one cluster (up to 8192 tokens): the multi-pass form of the pass
+    "prefill_long": Workload("prefill_long", 6, 16, 32, 32, 8, 128, 16, 128, 32, key_recipe="clustered",
+                             prefill_max=8192),
 }
 
 
