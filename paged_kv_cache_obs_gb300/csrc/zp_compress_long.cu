@@ -410,10 +410,12 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
 }
 
 // 4. In-place compaction of the moved K and V rows, one CTA per unit, 128 source rows at a time.
+//    Each chunk first records, per row, the byte offsets of its source and destination rows
+//    (or -1), so that the copy loops issue independent loads and stores.
 __global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressArgs a, const LongScratch sc) {
   extern __shared__ uint8_t smem_raw[];
   uint4* stage = reinterpret_cast<uint4*>(smem_raw);  // [kCompactRows][2 * d / 8] 16-byte pieces
-  __shared__ int moved_dst[kCompactRows];
+  __shared__ long long src_off[kCompactRows], dst_off[kCompactRows];
   const int tid = threadIdx.x;
   const int unit = blockIdx.x;
   const UnitMeta m = unit_meta(a, unit);
@@ -423,34 +425,41 @@ __global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressAr
   const int32_t* dst_tab = a.dst_tables + static_cast<int64_t>(m.r) * a.max_blocks;
   uint8_t* const head_base = a.pool + static_cast<size_t>(m.layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
                              static_cast<size_t>(m.h) * a.b * a.row_bytes;
-  const int bm = a.b - 1, pieces = 2 * a.d / 8;  // 16-byte pieces of a row's K and V
+  const int bm = a.b - 1;
+  const int half = a.d / 8;        // 16-byte pieces of a K (or V) row
+  const int pieces = 2 * half;     // K then V
   for (int c0 = 0; c0 < m.L; c0 += kCompactRows) {
     if (tid < kCompactRows) {
       const int t = c0 + tid;
-      int md = -1;
+      long long so = -1, dso = -1;
       if (t < m.L) {
         const int jj = dst[t];  // -1 for an evicted key (or a reported unit)
-        if (jj >= 0 && (src_tab[t >> a.b_shift] != dst_tab[jj >> a.b_shift] || (t & bm) != (jj & bm))) md = jj;
+        if (jj >= 0) {
+          const int sb = src_tab[t >> a.b_shift], db = dst_tab[jj >> a.b_shift];
+          if (sb != db || (t & bm) != (jj & bm)) {
+            so = static_cast<long long>(static_cast<uint32_t>(sb)) * a.block_bytes + static_cast<uint32_t>(t & bm) * a.row_bytes;
+            dso = static_cast<long long>(static_cast<uint32_t>(db)) * a.block_bytes + static_cast<uint32_t>(jj & bm) * a.row_bytes;
+          }
+        }
       }
-      moved_dst[tid] = md;
+      src_off[tid] = so;
+      dst_off[tid] = dso;
     }
     __syncthreads();
-    for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
-      const int row = i / pieces, pc = i % pieces, t = c0 + row;
-      if (moved_dst[row] < 0) continue;
-      const int kv = pc >= pieces / 2, off = (pc % (pieces / 2)) * 16;
-      stage[i] = *reinterpret_cast<const uint4*>(
-          head_base + static_cast<size_t>(static_cast<uint32_t>(src_tab[t >> a.b_shift])) * a.block_bytes +
-          kv * a.kv_bytes + static_cast<uint32_t>(t & bm) * a.row_bytes + off);
-    }
-    __syncthreads();  // every read of the chunk precedes every write landing on it
+#pragma unroll 4
     for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
       const int row = i / pieces, pc = i % pieces;
-      const int jj = moved_dst[row];
-      if (jj < 0) continue;
-      const int kv = pc >= pieces / 2, off = (pc % (pieces / 2)) * 16;
-      *reinterpret_cast<uint4*>(head_base + static_cast<size_t>(static_cast<uint32_t>(dst_tab[jj >> a.b_shift])) * a.block_bytes +
-                                kv * a.kv_bytes + static_cast<uint32_t>(jj & bm) * a.row_bytes + off) = stage[i];
+      const long long so = src_off[row];
+      if (so < 0) continue;
+      stage[i] = *reinterpret_cast<const uint4*>(head_base + so + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16);
+    }
+    __syncthreads();  // every read of the chunk precedes every write landing on it
+#pragma unroll 4
+    for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
+      const int row = i / pieces, pc = i % pieces;
+      const long long dso = dst_off[row];
+      if (dso < 0) continue;
+      *reinterpret_cast<uint4*>(head_base + dso + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16) = stage[i];
     }
     __syncthreads();
   }
