@@ -338,9 +338,11 @@ def run_e2e(args, wl, inp, pristine_pool, pristine_gs, world):
     import numpy as np
     import torch
     from paged_kv_cache_obs_gb300 import runner, zipage
+    # the host-resident pool: each step copies it in, compresses, and copies the compacted pool
+    # back into the same buffer (one pinned copy per rank keeps the footprint at one pool)
     h_pool = torch.empty(pristine_pool.shape, dtype=pristine_pool.dtype, pin_memory=True)
     h_pool.copy_(pristine_pool)
-    h_out = torch.empty_like(h_pool, pin_memory=True)
+    h_out = h_pool
     h_q = inp.obs_q.cpu().pin_memory()
     h_gs = pristine_gs.cpu().pin_memory()
     h_gs_out = torch.empty_like(h_gs, pin_memory=True)
