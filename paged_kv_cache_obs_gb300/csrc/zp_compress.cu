@@ -739,6 +739,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
                                  const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
                                  const zp_params* p, const zp_debug* dbg, void* workspace,
                                  size_t workspace_bytes, zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_compress");
   if (!pool || !meta || !obs_q || !global_scores || !p || !workspace) return ZP_ERR_INVALID_ARG;
   if (!pool->base || pool->num_blocks <= 0) return ZP_ERR_INVALID_ARG;
   // with no request the per-request arrays may be empty (NULL)

@@ -404,6 +404,7 @@ extern "C" zp_status zp_paged_decode_attn(const zp_kv_pool* pool, int32_t layer,
                                           const int32_t* block_tables, const int32_t* seq_lens, int32_t B,
                                           int32_t max_blocks, uint16_t* out, const zp_params* p, void* workspace,
                                           size_t workspace_bytes, zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_paged_decode_attn");
   zp_status s = decode_validate(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p);
   if (s != ZP_OK) return s;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < zp_paged_decode_workspace_size(p, B, max_blocks))
@@ -436,6 +437,7 @@ extern "C" zp_status zp_paged_decode_attn_static(const zp_kv_pool* pool, int32_t
                                                  const int32_t* block_tables, const int32_t* seq_lens,
                                                  int32_t B, int32_t max_blocks, uint16_t* out,
                                                  const zp_params* p, int32_t* dev_status, zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_paged_decode_attn_static");
   zp_status s = decode_validate(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p);
   if (s != ZP_OK) return s;
   const size_t need = zp_paged_decode_workspace_size(p, B, max_blocks) - 256;  // partials only

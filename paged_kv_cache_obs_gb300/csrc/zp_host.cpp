@@ -299,12 +299,14 @@ zp_status commit_impl(zp_alloc* a, const int32_t* old_tables, const int32_t* new
 
 zp_status zp_plan_compress(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks, int32_t n_max,
                            int32_t* host_dst_tables) {
+  zp::NvtxRange nvtx_range("zp_plan_compress");
   if (n_max < 2 || max_blocks < n_max) return ZP_ERR_INVALID_ARG;
   return plan_impl(a, host_tables, R, max_blocks, nullptr, n_max, host_dst_tables);
 }
 
 zp_status zp_plan_compress_budgets(zp_alloc* a, const int32_t* host_tables, int32_t R, int32_t max_blocks,
                                    const int32_t* host_n_max, int32_t* host_dst_tables) {
+  zp::NvtxRange nvtx_range("zp_plan_compress_budgets");
   if (!host_n_max && R > 0) return ZP_ERR_INVALID_ARG;
   return plan_impl(a, host_tables, R, max_blocks, host_n_max, 0, host_dst_tables);
 }
@@ -312,6 +314,7 @@ zp_status zp_plan_compress_budgets(zp_alloc* a, const int32_t* host_tables, int3
 zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R,
                              int32_t max_blocks, int32_t n_max, int32_t block_size, const int32_t* host_seq_len,
                              zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_commit_compress");
   if (n_max < 2 || max_blocks < n_max) return ZP_ERR_INVALID_ARG;
   return commit_impl(a, old_tables, new_tables, R, max_blocks, nullptr, n_max, block_size, host_seq_len, stream);
 }
@@ -319,6 +322,7 @@ zp_status zp_commit_compress(zp_alloc* a, const int32_t* old_tables, const int32
 zp_status zp_commit_compress_budgets(zp_alloc* a, const int32_t* old_tables, const int32_t* new_tables, int32_t R,
                                      int32_t max_blocks, const int32_t* host_n_max, int32_t n_max, int32_t block_size,
                                      const int32_t* host_seq_len, zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_commit_compress_budgets");
   return commit_impl(a, old_tables, new_tables, R, max_blocks, host_n_max, n_max, block_size, host_seq_len, stream);
 }
 

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/zipage.h"
 
@@ -20,5 +21,14 @@ bool encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64
 int num_sms();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// NVTX range over the host side of an entry point (a no-op unless a profiler listens), so
+// that a timeline shows which call queued which kernels.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace zp

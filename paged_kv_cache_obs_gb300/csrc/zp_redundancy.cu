@@ -286,6 +286,7 @@ extern "C" size_t zp_redundancy_workspace_size(const zp_params* p, int32_t num_r
 extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32_t* block_tables,
                                              const zp_seq_meta* meta, const zp_params* p, float* redund,
                                              void* workspace, size_t workspace_bytes, zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_redundancy_all_pairs");
   if (!pool || !meta || !p || !workspace) return ZP_ERR_INVALID_ARG;
   if (!pool->base || pool->num_blocks <= 0) return ZP_ERR_INVALID_ARG;
   const int R = meta->num_requests;
