@@ -44,7 +44,7 @@ enum {
   ZP_ERR_BAD_TABLE = 3,    /* (device) a block id, seq_len or query slot is out of range */
   ZP_ERR_TIMEOUT = 4,      /* (device) a bounded wait inside a kernel gave up */
   ZP_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
-  ZP_ERR_UNSUPPORTED = 6,  /* valid arguments outside what this build implements */
+  ZP_ERR_UNSUPPORTED = 6,  /* valid arguments outside what the library implements */
   ZP_ERR_TOO_LARGE = 7     /* the call needs more scratch than zp_paged_decode_attn_static holds */
 };
 

@@ -23,7 +23,7 @@ for LLM Reasoning through Compressed PagedAttention", arXiv 2603.08743, on gist.
 * de page, section 2 ("Lightning Redundancy Score"): the redundancy is computed block by
   block without materialising the full similarity matrix.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * scale = 1/sqrt(d) (the usual attention scale);
 * the observation-window query i is the query of token position L-w+i and attends causally,
