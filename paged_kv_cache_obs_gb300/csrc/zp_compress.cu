@@ -491,22 +491,30 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
     }
   } else {
     // Many evictions (the first compression after a long prefill): every CTA sorts its 256
-    // keys (bitonic network in shared memory); after a cluster barrier each key counts the
-    // smaller keys of every CTA by binary search in that CTA's sorted list (DSMEM).
-    if (!skip) lst[tid] = mykey;
-    __syncthreads();
-    for (int k2 = 2; k2 <= kKeysPerCta; k2 <<= 1)
-      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-        if (!skip && tid < kKeysPerCta / 2) {
-          const int i = 2 * tid - (tid & (j2 - 1));
-          const unsigned long long x = lst[i], y = lst[i + j2];
-          if ((x > y) == ((i & k2) == 0)) {
-            lst[i] = y;
-            lst[i + j2] = x;
+    // keys (bitonic network: partners within a warp by shuffles, across warps through shared
+    // memory); after a cluster barrier each key counts the smaller keys of every CTA by binary
+    // search in that CTA's sorted list (DSMEM).
+    if (!skip) {  // uniform over the CTA
+      unsigned long long x = mykey;
+#pragma unroll
+      for (int k2 = 2; k2 <= kKeysPerCta; k2 <<= 1)
+#pragma unroll
+        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+          unsigned long long y;
+          if (j2 >= 32) {
+            lst[tid] = x;
+            __syncthreads();
+            y = lst[tid ^ j2];
+            __syncthreads();
+          } else {
+            y = __shfl_xor_sync(0xffffffffu, x, j2);
           }
+          // the lower index of a pair keeps the smaller key in an ascending run
+          const bool keep_min = ((tid & j2) == 0) == ((tid & k2) == 0);
+          x = keep_min ? (x < y ? x : y) : (x < y ? y : x);
         }
-        __syncthreads();
-      }
+      lst[tid] = x;
+    }
     cluster_sync();  // every CTA's sorted list is complete
     if (!skip && key_valid) {
       int pos[MAXC];
