@@ -44,8 +44,7 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         if ptxas_info and src.endswith(".cu"):
             cmd += ["-Xptxas", "-v"]
         if src.endswith(".cpp"):
-            cmd = [nvcc, *COMMON, "-x", "cu", "-c", src, "-o", obj] if False else \
-                  [nvcc, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+            cmd = [nvcc, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{res.stdout}\n{res.stderr}")

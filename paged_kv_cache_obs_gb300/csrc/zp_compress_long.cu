@@ -11,8 +11,9 @@
 //   3. select:  per unit: the E = L - k lowest eviction keys by an 8-pass radix select of the
 //               64-bit keys (order(S), ~t), destinations by a block-wide scan, and the global
 //               scores updated in place (every read before any write);
-//   4. compact: per unit: the moved K and V rows, 128 source rows at a time in increasing
-//               order (dst <= src, so a chunk's rows are read before anything lands on them).
+//   4. compact: per unit: the moved K and V rows, 128 destination slots at a time in
+//               increasing order (dst <= src, so a chunk's rows are read before anything lands
+//               on them).
 // Every wait is bounded.  A unit with bad metadata or block ids is reported and left untouched.
 #include <algorithm>
 #include <mutex>
@@ -31,7 +32,7 @@ struct LongScratch {
   float* attn;   // [units][L]
   float* red;    // [units][L]
   float* score;  // [units][L]
-  int32_t* dst;  // [units][L]: destination slot of each kept key, -1 if evicted
+  int32_t* src;  // [units][L]: source position of each destination slot j < k (-1: a reported unit)
   int nch;       // 256-key chunks per unit at the launch length
 };
 
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = blockIdx.x;
   const UnitMeta m = unit_meta(a, unit);
-  int32_t* dst = sc.dst + static_cast<int64_t>(unit) * a.L;
+  int32_t* src = sc.src + static_cast<int64_t>(unit) * a.L;
   if (tid == 0) bad_s = m.bad ? 1 : 0;
   __syncthreads();
   if (!m.bad) {  // every block id the unit reads or writes
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   __syncthreads();
   if (bad_s) {  // reported; the unit keeps its pool rows and global scores
     if (tid == 0) record_error(a.err, ZP_ERR_BAD_TABLE);
-    for (int t = tid; t < a.L; t += kSelThreads) dst[t] = -1;
+    for (int t = tid; t < a.L; t += kSelThreads) src[t] = -1;
     return;
   }
   const int L = m.L, E = L - m.k_r;
@@ -400,27 +401,32 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   for (int e = 0; e < kPer; ++e) {
     const int t = p0 + e;
     if (t >= a.L) break;
-    dst[t] = jdst[e];
     if (t >= L) continue;
-    if (jdst[e] >= 0) G[jdst[e]] = gnew[e];
+    if (jdst[e] >= 0) {
+      src[jdst[e]] = t;
+      G[jdst[e]] = gnew[e];
+    }
     if (a.dbg_keep) a.dbg_keep[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t] = jdst[e] >= 0;
   }
   __syncthreads();
   for (int t = m.k_r + tid; t < L; t += kSelThreads) G[t] = 0.0f;  // slots past the k survivors
 }
 
-// 4. In-place compaction of the moved K and V rows, one CTA per unit, 128 source rows at a time.
-//    Each chunk first records, per row, the byte offsets of its source and destination rows
-//    (or -1), so that the copy loops issue independent loads and stores.
+// 4. In-place compaction of the moved K and V rows, one CTA per unit, 128 destination slots at a
+//    time.  A row only moves to a lower slot (dst <= src), so the sources of the slots past a
+//    chunk all lie past that chunk: chunk by chunk in increasing order, with every read of a
+//    chunk before any of its writes, is a safe order, and every chunk is full of kept rows.  A
+//    chunk's 16-byte pieces are all loaded into registers at once (one memory round trip per
+//    chunk), and the next chunk's per-row byte offsets (source and destination, or -1 for a
+//    row that stays) are computed while those loads are in flight, into a ring of three offset
+//    buffers (a buffer is refilled only after the barrier that follows the writes that used it).
 __global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressArgs a, const LongScratch sc) {
-  extern __shared__ uint8_t smem_raw[];
-  uint4* stage = reinterpret_cast<uint4*>(smem_raw);  // [kCompactRows][2 * d / 8] 16-byte pieces
-  __shared__ long long src_off[kCompactRows], dst_off[kCompactRows];
+  __shared__ long long src_off[3][kCompactRows], dst_off[3][kCompactRows];
   const int tid = threadIdx.x;
   const int unit = blockIdx.x;
   const UnitMeta m = unit_meta(a, unit);
   if (m.bad) return;
-  const int32_t* dst = sc.dst + static_cast<int64_t>(unit) * a.L;
+  const int32_t* src = sc.src + static_cast<int64_t>(unit) * a.L;
   const int32_t* src_tab = a.block_tables + static_cast<int64_t>(m.r) * a.max_blocks;
   const int32_t* dst_tab = a.dst_tables + static_cast<int64_t>(m.r) * a.max_blocks;
   uint8_t* const head_base = a.pool + static_cast<size_t>(m.layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
@@ -428,40 +434,54 @@ __global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressAr
   const int bm = a.b - 1;
   const int half = a.d / 8;        // 16-byte pieces of a K (or V) row
   const int pieces = 2 * half;     // K then V
-  for (int c0 = 0; c0 < m.L; c0 += kCompactRows) {
+  const int total = kCompactRows * pieces;
+  auto offsets = [&](int j0, int buf) {  // threads 0..127: byte offsets of slot j0 + tid
     if (tid < kCompactRows) {
-      const int t = c0 + tid;
+      const int j = j0 + tid;
       long long so = -1, dso = -1;
-      if (t < m.L) {
-        const int jj = dst[t];  // -1 for an evicted key (or a reported unit)
-        if (jj >= 0) {
-          const int sb = src_tab[t >> a.b_shift], db = dst_tab[jj >> a.b_shift];
-          if (sb != db || (t & bm) != (jj & bm)) {
+      if (j < m.k_r) {
+        const int t = src[j];  // -1 for a reported unit
+        if (t >= 0) {
+          const int sb = src_tab[t >> a.b_shift], db = dst_tab[j >> a.b_shift];
+          if (sb != db || (t & bm) != (j & bm)) {
             so = static_cast<long long>(static_cast<uint32_t>(sb)) * a.block_bytes + static_cast<uint32_t>(t & bm) * a.row_bytes;
-            dso = static_cast<long long>(static_cast<uint32_t>(db)) * a.block_bytes + static_cast<uint32_t>(jj & bm) * a.row_bytes;
+            dso = static_cast<long long>(static_cast<uint32_t>(db)) * a.block_bytes + static_cast<uint32_t>(j & bm) * a.row_bytes;
           }
         }
       }
-      src_off[tid] = so;
-      dst_off[tid] = dso;
+      src_off[buf][tid] = so;
+      dst_off[buf][tid] = dso;
     }
-    __syncthreads();
-#pragma unroll 4
-    for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
-      const int row = i / pieces, pc = i % pieces;
-      const long long so = src_off[row];
-      if (so < 0) continue;
-      stage[i] = *reinterpret_cast<const uint4*>(head_base + so + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16);
+  };
+  constexpr int kPer = kCompactRows * 2 * 128 / 8 / kThreads;  // pieces per thread at d = 128
+  offsets(0, 0);
+  __syncthreads();
+  int buf = 0;
+  for (int c0 = 0; c0 < m.k_r; c0 += kCompactRows) {
+    uint4 v[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int i = tid + q * kThreads;
+      v[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < total) {
+        const int row = i / pieces, pc = i % pieces;
+        const long long so = src_off[buf][row];
+        if (so >= 0) v[q] = *reinterpret_cast<const uint4*>(head_base + so + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16);
+      }
     }
-    __syncthreads();  // every read of the chunk precedes every write landing on it
-#pragma unroll 4
-    for (int i = tid; i < kCompactRows * pieces; i += kThreads) {
-      const int row = i / pieces, pc = i % pieces;
-      const long long dso = dst_off[row];
-      if (dso < 0) continue;
-      *reinterpret_cast<uint4*>(head_base + dso + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16) = stage[i];
+    const int nbuf = buf == 2 ? 0 : buf + 1;
+    if (c0 + kCompactRows < m.k_r) offsets(c0 + kCompactRows, nbuf);
+    __syncthreads();  // every read of this chunk precedes every write landing on it
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int i = tid + q * kThreads;
+      if (i < total) {
+        const int row = i / pieces, pc = i % pieces;
+        const long long dso = dst_off[buf][row];
+        if (dso >= 0) *reinterpret_cast<uint4*>(head_base + dso + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16) = v[q];
+      }
     }
-    __syncthreads();
+    buf = nbuf;
   }
 }
 
@@ -489,26 +509,22 @@ zp_status launch_compress_long(const CUtensorMap& tmK, const CUtensorMap& tmQ, c
   p += static_cast<size_t>(units) * a.L * 4;
   sc.score = reinterpret_cast<float*>(p);
   p += static_cast<size_t>(units) * a.L * 4;
-  sc.dst = reinterpret_cast<int32_t*>(p);
+  sc.src = reinterpret_cast<int32_t*>(p);
   if (units * sc.nch >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
   const size_t smem = sizeof(LongSmem) + 1024;
-  const size_t cmp_smem = static_cast<size_t>(kCompactRows) * 2 * a.d * 2;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(long_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (attr == cudaSuccess)
       attr = cudaFuncSetAttribute(long_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(long_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kCompactRows * 2 * 128 * 2);
   });
   if (attr != cudaSuccess) return ZP_ERR_CUDA;
   const unsigned chunks = static_cast<unsigned>(units * sc.nch);
   long_stats_kernel<<<chunks, kThreads, smem, st>>>(tmK, tmQ, a, sc);
   long_score_kernel<<<chunks, kThreads, smem, st>>>(tmK, tmQ, a, sc);
   long_select_kernel<<<static_cast<unsigned>(units), kSelThreads, 0, st>>>(a, sc);
-  long_compact_kernel<<<static_cast<unsigned>(units), kThreads, cmp_smem, st>>>(a, sc);
+  long_compact_kernel<<<static_cast<unsigned>(units), kThreads, 0, st>>>(a, sc);
   return cudaGetLastError() == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
 }
 
