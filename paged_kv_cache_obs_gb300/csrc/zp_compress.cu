@@ -51,8 +51,8 @@ struct __align__(1024) SmemT {
   union {
     float2 recv[MAXC][kRows];                   // (max, sum) partials of every CTA
     struct {
-      unsigned long long key[kKeysPerCta];      // eviction keys of this CTA
-      unsigned long long wcand[kKeysPerCta];    // per-warp candidates
+      unsigned long long key[kKeysPerCta];      // eviction keys of this CTA (sorted on the many-eviction path)
+      unsigned long long copy[kKeysPerCta];     // local copy of another CTA's sorted keys
     } sel;
   } u1;
   unsigned long long cand_recv[MAXC * 32];  // sorted bottom-32 list of every CTA
@@ -77,6 +77,7 @@ struct __align__(1024) SmemT {
 // 1 KB alignment slack of the dynamic allocation
 static_assert(sizeof(SmemT<8>) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "8-CTA clusters: two CTAs per SM");
 static_assert(sizeof(SmemT<16>) + 1024 <= 227 * 1024, "16-CTA clusters: one CTA per SM");
+static_assert(sizeof(SmemT<8>::cand_recv) >= kKeysPerCta * 8, "a copied key list fits the candidate lists");
 
 // Sorts one 64-bit key per lane ascending across the warp (bitonic network).
 __device__ __forceinline__ unsigned long long warp_sort32(unsigned long long x, int lane) {
@@ -492,8 +493,10 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
   } else {
     // Many evictions (the first compression after a long prefill): every CTA sorts its 256
     // keys (bitonic network: partners within a warp by shuffles, across warps through shared
-    // memory); after a cluster barrier each key counts the smaller keys of every CTA by binary
-    // search in that CTA's sorted list (DSMEM).
+    // memory).  After a cluster barrier every CTA copies the sorted lists of the cluster into
+    // its own shared memory (one coalesced remote load per thread and list, all issued at
+    // once), two lists at a time, and each key counts the smaller keys of each list by binary
+    // search there.
     if (!skip) {  // uniform over the CTA
       unsigned long long x = mykey;
 #pragma unroll
@@ -516,24 +519,33 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
       lst[tid] = x;
     }
     cluster_sync();  // every CTA's sorted list is complete
-    if (!skip && key_valid) {
-      int pos[MAXC];
-      uint32_t base[MAXC];
+    if (!skip) {  // uniform over the CTA
+      unsigned long long rk[MAXC];
+      const uint32_t mine = smem_u32(&lst[tid]);
 #pragma unroll
-      for (int cc = 0; cc < MAXC; ++cc) {
-        pos[cc] = 0;
-        base[cc] = mapa(smem_u32(lst), cc < C ? cc : 0);
-      }
-#pragma unroll
-      for (int step = kKeysPerCta / 2; step > 0; step >>= 1)
-#pragma unroll
-        for (int cc = 0; cc < MAXC; ++cc)
-          if (cc < C && ld_cluster_u64(base[cc] + 8u * static_cast<uint32_t>(pos[cc] + step - 1)) < mykey)
-            pos[cc] += step;
+      for (int cc = 0; cc < MAXC; ++cc) rk[cc] = cc < C ? ld_cluster_u64(mapa(mine, cc)) : 0ull;
+      // local buffers: nothing else uses them on this path between the sort and barrier #2
+      // (the candidate lists belong to the few-eviction path, u0 to passes 1 and the merge)
+      unsigned long long* const buf0 = s.u1.sel.copy;
+      unsigned long long* const buf1 = s.cand_recv;
       int rank = 0;
 #pragma unroll
-      for (int cc = 0; cc < MAXC; ++cc) rank += (cc < C) ? pos[cc] : 0;
-      evicted = rank < E;
+      for (int cc = 0; cc < MAXC; cc += 2) {
+        if (cc >= C) break;  // C is uniform over the cluster
+        const bool two = cc + 1 < C;
+        buf0[tid] = rk[cc];
+        if (two) buf1[tid] = rk[cc + 1];
+        __syncthreads();
+        int p0 = 0, p1 = 0;
+#pragma unroll
+        for (int step = kKeysPerCta / 2; step > 0; step >>= 1) {
+          if (buf0[p0 + step - 1] < mykey) p0 += step;
+          if (two && buf1[p1 + step - 1] < mykey) p1 += step;
+        }
+        rank += p0 + p1;
+        __syncthreads();
+      }
+      evicted = key_valid && rank < E;
     }
     const int kept_cta = __syncthreads_count(!skip && key_valid && !evicted);
     if (!skip && tid == 0) {
