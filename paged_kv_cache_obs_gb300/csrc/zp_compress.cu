@@ -536,12 +536,16 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
         buf0[tid] = rk[cc];
         if (two) buf1[tid] = rk[cc + 1];
         __syncthreads();
+        // keys below mykey in each list: the halving steps reach 255 at most, the last
+        // compare counts the list's last key
         int p0 = 0, p1 = 0;
 #pragma unroll
         for (int step = kKeysPerCta / 2; step > 0; step >>= 1) {
           if (buf0[p0 + step - 1] < mykey) p0 += step;
           if (two && buf1[p1 + step - 1] < mykey) p1 += step;
         }
+        p0 += buf0[p0] < mykey ? 1 : 0;
+        if (two) p1 += buf1[p1] < mykey ? 1 : 0;
         rank += p0 + p1;
         __syncthreads();
       }

@@ -123,6 +123,23 @@ def test_exact_ties_keep_the_earlier_tokens(zp):
     batch.close()
 
 
+def test_lowest_scores_fill_whole_ctas(zp):
+    # first compressions after a prefill (E up to 972) whose 256 lowest scores are the keys of
+    # one CTA (CTA 0 for even heads, CTA 1 for odd ones): every kept key then ranks above the
+    # whole sorted list of that CTA, and its rank must count all 256 of them
+    wl = synth.WORKLOADS["prefill"].scaled(num_requests=6, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                           n_max=9, window=8, prefill_max=1100)
+
+    def mutate(inp):
+        assert sum(int(x) >= 128 + 512 for x in inp.seq_len) >= 2  # both CTAs full, E >= 256
+        for h in range(wl.num_kv_heads):
+            lo = 256 * (h % 2)
+            inp.global_scores[:, :, h, lo:lo + 256] = -10.0
+
+    ndiff = _check_all(zp, wl, mutate=mutate)
+    assert ndiff == 0
+
+
 def test_bad_block_id_skips_the_request_and_reports(zp):
     wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, n_max=16)
     zipage, runner = zp
