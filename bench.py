@@ -312,6 +312,19 @@ def _reset_alloc(batch, inp):
     batch.dst_tables = zipage.zp_plan_compress(batch.alloc, batch.tables, inp.wl.n_max)
 
 
+COMPRESS_SOURCES = ("zp_compress.cu", "zp_compress_common.cuh", "zp_ptx.cuh")
+
+
+def compress_source_sha256():
+    """sha256 over the sources compress_kernel is compiled from, in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in COMPRESS_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_obs_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _ncu_traffic(workload):
     """DRAM bytes per launch of compress_kernel from the committed ncu summary, if it exists
     and was taken on the current kernel source (else null)."""
@@ -319,9 +332,7 @@ def _ncu_traffic(workload):
     try:
         with open(path) as f:
             rec = json.load(f)
-        import hashlib
-        src = open(os.path.join(ROOT, "paged_kv_cache_obs_gb300", "csrc", "zp_compress.cu"), "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        if rec.get("source_sha256") != compress_source_sha256():
             return None
         return rec.get("dram_bytes_per_launch")
     except (OSError, ValueError):

@@ -140,6 +140,23 @@ def test_lowest_scores_fill_whole_ctas(zp):
     assert ndiff == 0
 
 
+def test_eviction_counts_at_the_path_boundaries(zp):
+    # one launch whose requests evict exactly E = 1, 31, 32 (the last few-eviction case), 33
+    # (the first many-eviction case), 256 and 257 tokens per head: each request's length is
+    # cut to k + E inside the blocks it already holds
+    wl = synth.WORKLOADS["prefill"].scaled(num_requests=6, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                           n_max=9, window=8, prefill_max=1100)
+    k = (wl.n_max - 1) * wl.block_size
+
+    def mutate(inp):
+        order = np.argsort(inp.seq_len[:6], kind="stable")
+        for r, e in zip(order, [1, 31, 32, 33, 256, 257]):
+            assert int(inp.seq_len[r]) >= k + e
+            inp.seq_len[r] = k + e
+
+    assert _check_all(zp, wl, mutate=mutate) == 0
+
+
 def test_bad_block_id_skips_the_request_and_reports(zp):
     wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, n_max=16)
     zipage, runner = zp
