@@ -315,13 +315,33 @@ def _reset_alloc(batch, inp):
 COMPRESS_SOURCES = ("zp_compress.cu", "zp_compress_common.cuh", "zp_ptx.cuh")
 
 
+def _code_lines(text):
+    """The lines of a C++/CUDA source without // comments, trailing blanks and empty lines."""
+    out = []
+    for line in text.splitlines():
+        quoted, cut = False, len(line)
+        for i, ch in enumerate(line):
+            if ch == '"' and (i == 0 or line[i - 1] != "\\"):
+                quoted = not quoted
+            elif not quoted and line.startswith("//", i):
+                cut = i
+                break
+        code = line[:cut].rstrip()
+        if code:
+            out.append(code)
+    return out
+
+
 def compress_source_sha256():
-    """sha256 over the sources compress_kernel is compiled from, in a fixed order."""
+    """sha256 over the code (comments and blank lines dropped) of the sources compress_kernel is
+    compiled from, in a fixed order: a comment edit keeps a traffic record valid, a code edit
+    does not."""
     import hashlib
     h = hashlib.sha256()
     for name in COMPRESS_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_obs_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_obs_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update("\n".join(_code_lines(f.read())).encode())
+            h.update(b"\0")
     return h.hexdigest()
 
 

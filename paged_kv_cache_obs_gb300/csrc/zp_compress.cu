@@ -22,9 +22,9 @@
 //      redundancy of its 32 keys with warp-level MMA (block Gram, diagonal = squared norms).
 //   4. MMA D2 = K Q^T (M=128 keys, N=128 rows): each thread owns one key and sums its
 //      normalised probabilities over the window rows without shuffles (pass 2).
-//   5. Selection of the E = L-k lowest (S asc, t desc) keys: per-warp bitonic sort and merge
-//      trees (E <= 32) or a shared-memory sort and DSMEM ranks (E > 32); every CTA derives the
-//      same eviction set.
+//   5. Selection of the E = L-k lowest (S asc, t desc) keys: per-warp bitonic sorts and merge
+//      trees (E <= 32), or a CTA-wide bitonic sort and ranks by binary search in local copies
+//      of every CTA's sorted list (E > 32); every CTA derives the same eviction set.
 //   6. V rows are staged (shared memory and registers) before a cluster barrier that separates
 //      every read of the unit from every write (compaction is in place, dst <= src); K rows are
 //      written from shared memory, V rows from the staging, G' from registers.

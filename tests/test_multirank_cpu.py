@@ -48,3 +48,12 @@ def test_single_rank_defaults():
     os.environ.pop("RANK", None)
     assert bench.dist_env()[:2] == (0, 1)
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_traffic_record_key_ignores_comments_only():
+    import bench
+    src = 'int a = 1;  // one\n// a comment line\n\nconst char* s = "x // y";\n'
+    assert bench._code_lines(src) == ["int a = 1;", 'const char* s = "x // y";']
+    assert bench._code_lines(src.replace("one", "two")) == bench._code_lines(src)
+    assert bench._code_lines(src.replace("= 1", "= 2")) != bench._code_lines(src)
+    assert len(bench.compress_source_sha256()) == 64
