@@ -3,11 +3,13 @@
 // long prompt, zh §2.1).  Same operation, readings and results as the fused pass
 // (zp_compress.cu), with the cluster's exchanges replaced by kernel boundaries and global
 // scratch (the workspace past its first 256 bytes):
-//   1. stats:   per (unit, 256-key chunk): TMA of K and Q, tcgen05 D1 = Q K^T into TMEM, each
-//               window row's (max, exp-sum) over the chunk's visible keys, and the Lightning
-//               redundancy of the chunk's keys (warp-level MMA);
-//   2. score:   per (unit, chunk): every row's normaliser from all chunks' partials, K and Q
-//               again, D2 = K Q^T, the attention mass of each key and S = attn + a*G - b*R;
+//   1. stats:   per 256-key chunk: TMA of K (and once per CTA Q), tcgen05 D1 = Q K^T into
+//               TMEM, each window row's (max, exp-sum) over the chunk's visible keys, and the
+//               Lightning redundancy of the chunk's keys (warp-level MMA);
+//   2. score:   per chunk: every row's normaliser from all chunks' partials, K again, D2 =
+//               K Q^T, the attention mass of each key and S = attn + a*G - b*R;
+//               (a CTA of these two kernels takes up to four consecutive chunks of one unit and
+//               copies each chunk's K while the previous chunk's TMEM pass runs)
 //   3. select:  per unit: the E = L - k lowest eviction keys by an 8-pass radix select of the
 //               64-bit keys (order(S), ~t), destinations by a block-wide scan, and the global
 //               scores updated in place (every read before any write);
@@ -34,6 +36,7 @@ struct LongScratch {
   float* score;  // [units][L]
   int32_t* src;  // [units][L]: source position of each destination slot j < k (-1: a reported unit)
   int nch;       // 256-key chunks per unit at the launch length
+  int ngrp;      // CTAs of the stats and score kernels per unit (groups of kChunksPerCta chunks)
 };
 
 struct __align__(1024) LongSmem {
@@ -65,37 +68,48 @@ __device__ __forceinline__ UnitMeta unit_meta(const CompressArgs& a, int unit) {
   return m;
 }
 
-// TMA of the chunk's K blocks and the unit's window queries, D1 or D2 on tcgen05, shared by the
-// stats and score kernels.  Returns false if a bounded wait gave up.  (tid 0)
-__device__ __forceinline__ bool load_kq(LongSmem& s, const CUtensorMap* tmK, const CUtensorMap* tmQ,
-                                        const CompressArgs& a, const UnitMeta& m, const int* phys, int nblk,
-                                        uint32_t& ph_tma) {
+// A CTA of the stats and score kernels takes a group of up to kChunksPerCta consecutive chunks
+// of one unit: the window queries, the mbarriers, TMEM and the block ids load once, and each
+// chunk's K is copied while the previous chunk's TMEM pass runs.
+constexpr int kChunksPerCta = 4;
+constexpr int kGroupBlocks = kChunksPerCta * kKeysPerCta / 16;  // block ids of a group (b >= 16)
+
+// TMA of one chunk's K blocks (tid 0); the first chunk of a CTA also brings the window queries.
+__device__ __forceinline__ void issue_chunk_tma(LongSmem& s, const CUtensorMap* tmK, const CUtensorMap* tmQ,
+                                                const CompressArgs& a, const UnitMeta& m, const int* phys, int nblk,
+                                                bool with_q) {
   const int nhalf = a.d / 64;
-  mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>(((nblk << a.b_shift) + a.Rw) * a.d * 2));
-  for (int hd = 0; hd < nhalf; ++hd)
-    tma_load_3d(&s.Q[hd][0], tmQ, &s.bar_tma, hd * 64, m.h * a.Gq, (m.slot * a.layers + m.layer) * a.w);
+  mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>(((nblk << a.b_shift) + (with_q ? a.Rw : 0)) * a.d * 2));
+  if (with_q)
+    for (int hd = 0; hd < nhalf; ++hd)
+      tma_load_3d(&s.Q[hd][0], tmQ, &s.bar_tma, hd * 64, m.h * a.Gq, (m.slot * a.layers + m.layer) * a.w);
   for (int bi = 0; bi < nblk; ++bi)
     for (int hd = 0; hd < nhalf; ++hd)
       tma_load_3d(&s.K[hd][bi * a.b * 128], tmK, &s.bar_tma, hd * 64, m.h * a.b,
                   m.layer * static_cast<int>(a.num_blocks) + phys[bi]);
-  const bool ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
-  if (ok) ph_tma ^= 1;
-  return ok;
 }
 
-// Common prologue of the stats and score kernels: the chunk's block ids (checked), mbarriers,
-// TMEM, zeroed Q padding rows.  Returns the number of blocks, or -1 if the chunk has no work.
-__device__ __forceinline__ int chunk_prologue(LongSmem& s, const CompressArgs& a, const UnitMeta& m, int t0,
-                                              int* phys, int tid) {
-  const int nk = max(0, min(kKeysPerCta, m.L - t0));
-  if (m.bad || nk == 0) return -1;  // uniform over the CTA
-  const int nblk = (nk + a.b - 1) >> a.b_shift;
+// Chunks [c0, c1) of the unit that this CTA takes (c1 <= c0: none).
+__device__ __forceinline__ void group_range(const LongScratch& sc, const UnitMeta& m, int g, int& c0, int& c1) {
+  c0 = g * kChunksPerCta;
+  c1 = m.bad ? c0 : min(c0 + kChunksPerCta, (m.L + kKeysPerCta - 1) / kKeysPerCta);
+}
+
+__device__ __forceinline__ int chunk_keys(const UnitMeta& m, int c) { return min(kKeysPerCta, m.L - c * kKeysPerCta); }
+
+// Common prologue of the stats and score kernels for chunks [c0, c1) (c1 > c0): the group's
+// block ids (checked), mbarriers, zeroed Q padding rows.  Returns false if a block id is bad
+// (the select kernel reports the unit).
+__device__ __forceinline__ bool group_prologue(LongSmem& s, const CompressArgs& a, const UnitMeta& m, int c0, int c1,
+                                               int* phys, int tid) {
+  const int b0 = (c0 * kKeysPerCta) >> a.b_shift;
+  const int nb = (min(m.L, c1 * kKeysPerCta) - c0 * kKeysPerCta + a.b - 1) >> a.b_shift;  // <= kGroupBlocks
   __shared__ int bad_blk;
   if (tid == 0) bad_blk = 0;
   __syncthreads();
-  if (tid < nblk) {
-    const int p = a.block_tables[static_cast<int64_t>(m.r) * a.max_blocks + (t0 >> a.b_shift) + tid];
-    phys[tid] = p;
+  for (int i = tid; i < nb; i += kThreads) {
+    const int p = a.block_tables[static_cast<int64_t>(m.r) * a.max_blocks + b0 + i];
+    phys[i] = p;
     if (p < 0 || p >= a.num_blocks) bad_blk = 1;
   }
   if (tid == 0) {
@@ -109,115 +123,156 @@ __device__ __forceinline__ int chunk_prologue(LongSmem& s, const CompressArgs& a
   }
   fence_proxy_async_smem();
   __syncthreads();
-  if (bad_blk) return -1;  // reported by the select kernel
-  return nblk;
+  return !bad_blk;
 }
 
-// 1. Row statistics over the chunk and Lightning redundancy of its keys.
+// 1. Row statistics over each chunk and Lightning redundancy of its keys.  Per chunk: D1 on the
+//    tensor cores while the warps compute the redundancy (the last reads of K), the next
+//    chunk's TMA, then pass 1 over TMEM.
 __global__ void __launch_bounds__(kThreads, 2)
     long_stats_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                       const CompressArgs a, const LongScratch sc) {
   extern __shared__ uint8_t smem_raw[];
   LongSmem& s = *reinterpret_cast<LongSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ int phys[kKeysPerCta / 16];
+  __shared__ int phys[kGroupBlocks];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, hh = warp >> 2;
-  const int unit = static_cast<int>(blockIdx.x) / sc.nch, ch = static_cast<int>(blockIdx.x) % sc.nch;
-  const int t0 = ch * kKeysPerCta;
+  const int unit = static_cast<int>(blockIdx.x) / sc.ngrp, g = static_cast<int>(blockIdx.x) % sc.ngrp;
   const UnitMeta m = unit_meta(a, unit);
-  float2* part = sc.part + (static_cast<int64_t>(unit) * sc.nch + ch) * kRows;
-  const int nblk = chunk_prologue(s, a, m, t0, phys, tid);
-  if (nblk < 0) {
-    if (tid < kRows) part[tid] = make_float2(-INFINITY, 0.0f);
+  float2* const pu = sc.part + static_cast<int64_t>(unit) * sc.nch * kRows;
+  int c0, c1;
+  group_range(sc, m, g, c0, c1);
+  // chunks of this group (at the launch length) past the unit's end hold no keys
+  if (tid < kRows)
+    for (int c = max(c0, c1); c < min(g * kChunksPerCta + kChunksPerCta, sc.nch); ++c)
+      pu[c * kRows + tid] = make_float2(-INFINITY, 0.0f);
+  if (c1 <= c0) return;
+  if (!group_prologue(s, a, m, c0, c1, phys, tid)) {
+    if (tid < kRows)
+      for (int c = c0; c < c1; ++c) pu[c * kRows + tid] = make_float2(-INFINITY, 0.0f);
     return;
   }
-  const int nk = min(kKeysPerCta, m.L - t0);
   if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  bool ok = true;
-  uint32_t ph_tma = 0;
+  bool ok = true, tma_pending = false;  // (tid 0)
+  uint32_t ph_tma = 0, ph_mma = 0;
   if (tid == 0) {
-    ok = load_kq(s, &tmK, &tmQ, a, m, phys, nblk, ph_tma);
+    issue_chunk_tma(s, &tmK, &tmQ, a, m, phys, (chunk_keys(m, c0) + a.b - 1) >> a.b_shift, true);
+    tma_pending = true;
+  }
+  bool fail = false;
+  int boff = 0;  // the chunk's first entry in phys
+  for (int c = c0; c < c1 && !fail; ++c) {
+    const int t0 = c * kKeysPerCta;
+    const int nk = chunk_keys(m, c);
+    const int nblk = (nk + a.b - 1) >> a.b_shift;
+    if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
+      if (ok) {
+        ph_tma ^= 1;
+        tma_pending = false;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, (nk + 15) & ~15);
+        for (int kk = 0; kk < a.d / 16; ++kk)
+          mma_bf16(tbase, smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32])),
+                   smem_desc_sw128(smem_u32(&s.K[kk >> 2][(kk & 3) * 32])), idesc, kk > 0);
+        mma_commit(&s.bar_mma);
+      }
+    }
+    fail = __syncthreads_or(!ok);  // the chunk's K has landed; D1 runs during the redundancy
+    if (fail) break;
+    if (warp * 32 < nk) {
+      const float red = (a.b == 16) ? warp_lightning_redundancy<16>(s.K, s.inv_n, warp * 32, lane, a.d, t0, m.L)
+                                    : warp_lightning_redundancy<32>(s.K, s.inv_n, warp * 32, lane, a.d, t0, m.L);
+      if (tid < nk) {
+        const int64_t o = static_cast<int64_t>(unit) * a.L + t0 + tid;
+        sc.red[o] = red;
+        if (a.dbg_redund) a.dbg_redund[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t0 + tid] = red;
+      }
+    }
+    if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs);
+      ph_mma ^= 1;
+    }
+    // every read of K (the MMA and the redundancy) precedes the next chunk's TMA
+    fence_proxy_async_smem();
+    fail = __syncthreads_or(!ok);
     tc_fence_after();
-    const uint32_t idesc = idesc_bf16_f32(128, (nk + 15) & ~15);
-    for (int kk = 0; kk < a.d / 16; ++kk)
-      mma_bf16(tbase, smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32])),
-               smem_desc_sw128(smem_u32(&s.K[kk >> 2][(kk & 3) * 32])), idesc, kk > 0);
-    mma_commit(&s.bar_mma);
-    ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
-  }
-  const bool fail = __syncthreads_or(!ok);
-  tc_fence_after();
-  if (!fail) {
-    // thread = window row i, warp half hh = 128 key columns; keys t <= L-w+i/G_q are visible
-    const int i = q4 * 32 + lane;
-    const int cbase = hh * 128, ncol = nk - cbase;
-    const int vlim = max(0, min(ncol, (a.causal ? (m.L - a.w + i / a.Gq) : (m.L - 1)) - t0 - cbase + 1));
-    const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
-    float mx = -INFINITY, ls = 0.0f;
-    for (int c2 = 0; c2 < 4 && c2 * 32 < ncol; ++c2) {
-      float v[32];
-      tmem_ld32(tl + c2 * 32, v);
-      float cm = mx;
+    if (fail) break;
+    if (tid == 0 && c + 1 < c1) {
+      issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false);
+      tma_pending = true;
+    }
+    boff += nblk;
+    {
+      // pass 1: thread = window row i, warp half hh = 128 key columns; keys t <= L-w+i/G_q
+      // are visible
+      const int i = q4 * 32 + lane;
+      const int cbase = hh * 128, ncol = nk - cbase;
+      const int vlim = max(0, min(ncol, (a.causal ? (m.L - a.w + i / a.Gq) : (m.L - 1)) - t0 - cbase + 1));
+      const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
+      float mx = -INFINITY, ls = 0.0f;
+      for (int c2 = 0; c2 < 4 && c2 * 32 < ncol; ++c2) {
+        float v[32];
+        tmem_ld32(tl + c2 * 32, v);
+        float cm = mx;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c2 * 32 + j < vlim) cm = fmaxf(cm, v[j]);
-      if (cm == -INFINITY) continue;
-      if (mx != -INFINITY && cm > mx) ls *= ex2((mx - cm) * a.sl2);
-      mx = cm;
+        for (int j = 0; j < 32; ++j)
+          if (c2 * 32 + j < vlim) cm = fmaxf(cm, v[j]);
+        if (cm == -INFINITY) continue;
+        if (mx != -INFINITY && cm > mx) ls *= ex2((mx - cm) * a.sl2);
+        mx = cm;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c2 * 32 + j < vlim) ls += ex2(fmaf(v[j], a.sl2, -mx * a.sl2));
+        for (int j = 0; j < 32; ++j)
+          if (c2 * 32 + j < vlim) ls += ex2(fmaf(v[j], a.sl2, -mx * a.sl2));
+      }
+      s.part[hh][i] = make_float2(mx, ls);
     }
-    s.part[hh][i] = make_float2(mx, ls);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (!fail && tid < kRows) {
-    const float2 p0 = s.part[0][tid], p1 = s.part[1][tid];
-    float mm = fmaxf(p0.x, p1.x), l = 0.0f;
-    if (tid >= a.Rw) mm = -INFINITY;  // a padding row of the MMA, not a window row
-    if (mm != -INFINITY) {
-      if (p0.y > 0.0f) l += p0.y * ex2((p0.x - mm) * a.sl2);
-      if (p1.y > 0.0f) l += p1.y * ex2((p1.x - mm) * a.sl2);
-    }
-    part[tid] = make_float2(mm, l);
-  } else if (fail && tid < kRows) {
-    part[tid] = make_float2(-INFINITY, 0.0f);
-  }
-  if (fail && tid == 0) record_error(a.err, ZP_ERR_TIMEOUT);
-  if (!fail && warp * 32 < nk) {
-    const float red = (a.b == 16) ? warp_lightning_redundancy<16>(s.K, s.inv_n, warp * 32, lane, a.d, t0, m.L)
-                                  : warp_lightning_redundancy<32>(s.K, s.inv_n, warp * 32, lane, a.d, t0, m.L);
-    if (tid < nk) {
-      const int64_t o = static_cast<int64_t>(unit) * a.L + t0 + tid;
-      sc.red[o] = red;
-      if (a.dbg_redund) a.dbg_redund[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t0 + tid] = red;
+    // every TMEM read of D1 precedes the next chunk's MMA
+    tc_fence_before();
+    __syncthreads();
+    if (tid < kRows) {
+      const float2 p0 = s.part[0][tid], p1 = s.part[1][tid];
+      float mm = fmaxf(p0.x, p1.x), l = 0.0f;
+      if (tid >= a.Rw) mm = -INFINITY;  // a padding row of the MMA, not a window row
+      if (mm != -INFINITY) {
+        if (p0.y > 0.0f) l += p0.y * ex2((p0.x - mm) * a.sl2);
+        if (p1.y > 0.0f) l += p1.y * ex2((p1.x - mm) * a.sl2);
+      }
+      pu[c * kRows + tid] = make_float2(mm, l);
     }
   }
+  if (fail) {
+    if (tid < kRows)
+      for (int c = c0; c < c1; ++c) pu[c * kRows + tid] = make_float2(-INFINITY, 0.0f);
+    if (tid == 0) record_error(a.err, ZP_ERR_TIMEOUT);
+  }
+  // a copy issued and never seen complete: wait (bounded) before the shared memory goes away
+  if (tid == 0 && tma_pending) mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-// 2. Attention mass of each key (every row normalised over all chunks) and its score S.
+// 2. Attention mass of each key (every row normalised over all chunks) and its score S.  Per
+//    chunk: D2 (the last read of K), the next chunk's TMA, then pass 2 over TMEM.
 __global__ void __launch_bounds__(kThreads, 2)
     long_score_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                       const CompressArgs a, const LongScratch sc) {
   extern __shared__ uint8_t smem_raw[];
   LongSmem& s = *reinterpret_cast<LongSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ int phys[kKeysPerCta / 16];
+  __shared__ int phys[kGroupBlocks];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int q4 = warp & 3, hh = warp >> 2;
-  const int unit = static_cast<int>(blockIdx.x) / sc.nch, ch = static_cast<int>(blockIdx.x) % sc.nch;
-  const int t0 = ch * kKeysPerCta;
+  const int unit = static_cast<int>(blockIdx.x) / sc.ngrp, g = static_cast<int>(blockIdx.x) % sc.ngrp;
   const UnitMeta m = unit_meta(a, unit);
-  const int nblk = chunk_prologue(s, a, m, t0, phys, tid);
-  if (nblk < 0) return;
-  const int nk = min(kKeysPerCta, m.L - t0);
+  int c0, c1;
+  group_range(sc, m, g, c0, c1);
+  if (c1 <= c0) return;
+  if (!group_prologue(s, a, m, c0, c1, phys, tid)) return;
   // every row's normaliser: log2 of its exp-sum over all chunks, relative to its max
   if (tid < kRows) {
     const float2* pu = sc.part + static_cast<int64_t>(unit) * sc.nch * kRows;
@@ -237,53 +292,83 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  bool ok = true;
-  uint32_t ph_tma = 0;
+  bool ok = true, tma_pending = false;  // (tid 0)
+  uint32_t ph_tma = 0, ph_mma = 0;
   if (tid == 0) {
-    ok = load_kq(s, &tmK, &tmQ, a, m, phys, nblk, ph_tma);
-    tc_fence_after();
-    const uint32_t idesc = idesc_bf16_f32(128, 128);
-    for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
-      for (int kk = 0; kk < a.d / 16; ++kk)
-        mma_bf16(tbase + kh * 128, smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32])),
-                 smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32])), idesc, kk > 0);
-    mma_commit(&s.bar_mma);
-    ok = mbar_wait_bounded(&s.bar_mma, 0, kWaitNs) && ok;
+    issue_chunk_tma(s, &tmK, &tmQ, a, m, phys, (chunk_keys(m, c0) + a.b - 1) >> a.b_shift, true);
+    tma_pending = true;
   }
-  const bool fail = __syncthreads_or(!ok);
-  tc_fence_after();
-  const int kt = t0 + tid;
-  const int wcol = hh * 128 + q4 * 32;
-  float attn = 0.0f;
-  if (!fail && wcol < nk) {
-    // thread = key (TMEM lane), columns = window rows; row i sees key kt iff kt <= L-w+i/G_q
-    const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128;
-    const int imin = a.causal ? max(0, a.Gq * (kt - (m.L - a.w))) : 0;
-    float acc = 0.0f;
-    for (int c2 = 0; c2 < 4 && c2 * 32 < a.Rw; ++c2) {
-      float v[32];
-      tmem_ld32(tl + c2 * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int row = c2 * 32 + j;
-        const float p = ex2(fmaf(v[j], a.sl2, -s.row_off[row]));
-        if (row >= imin) acc += p;
+  const int64_t gbase = ((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
+  const int64_t dbase = ((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
+  bool fail = false;
+  int boff = 0;
+  for (int c = c0; c < c1 && !fail; ++c) {
+    const int t0 = c * kKeysPerCta;
+    const int nk = chunk_keys(m, c);
+    const int nblk = (nk + a.b - 1) >> a.b_shift;
+    const int kt = t0 + tid;
+    // the global score and redundancy of this thread's key load while the chunk's copy runs
+    const float g_in = tid < nk ? a.gscores[gbase + kt] : 0.0f;
+    const float r_in = tid < nk ? sc.red[static_cast<int64_t>(unit) * a.L + kt] : 0.0f;
+    if (tid == 0) {
+      ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
+      if (ok) {
+        ph_tma ^= 1;
+        tma_pending = false;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, 128);
+        for (int kh = 0; kh < 2 && kh * 128 < nk; ++kh)
+          for (int kk = 0; kk < a.d / 16; ++kk)
+            mma_bf16(tbase + kh * 128, smem_desc_sw128(smem_u32(&s.K[kk >> 2][kh * 128 * 128 + (kk & 3) * 32])),
+                     smem_desc_sw128(smem_u32(&s.Q[kk >> 2][(kk & 3) * 32])), idesc, kk > 0);
+        mma_commit(&s.bar_mma);
+        ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs);
+        ph_mma ^= 1;
+        // the MMA has read K: the next chunk's copy may land while pass 2 runs
+        if (ok && c + 1 < c1) {
+          issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false);
+          tma_pending = true;
+        }
       }
     }
-    attn = acc * a.inv_rw;
-  }
-  if (!fail && tid < nk) {
-    const float g = a.gscores[((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L + kt];
-    const int64_t o = static_cast<int64_t>(unit) * a.L + kt;
-    float S = (attn + a.alpha * g) - a.beta * sc.red[o];
-    if (a.protect_window && kt >= m.L - a.w) S = INFINITY;
-    sc.attn[o] = attn;
-    sc.score[o] = S;
-    const int64_t od = ((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + kt;
-    if (a.dbg_attn) a.dbg_attn[od] = attn;
-    if (a.dbg_score) a.dbg_score[od] = S;
+    fail = __syncthreads_or(!ok);
+    tc_fence_after();
+    if (fail) break;
+    boff += nblk;
+    const int wcol = hh * 128 + q4 * 32;
+    float attn = 0.0f;
+    if (wcol < nk) {
+      // thread = key (TMEM lane), columns = window rows; row i sees key kt iff kt <= L-w+i/G_q
+      const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128;
+      const int imin = a.causal ? max(0, a.Gq * (kt - (m.L - a.w))) : 0;
+      float acc = 0.0f;
+      for (int c2 = 0; c2 < 4 && c2 * 32 < a.Rw; ++c2) {
+        float v[32];
+        tmem_ld32(tl + c2 * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int row = c2 * 32 + j;
+          const float p = ex2(fmaf(v[j], a.sl2, -s.row_off[row]));
+          if (row >= imin) acc += p;
+        }
+      }
+      attn = acc * a.inv_rw;
+    }
+    if (tid < nk) {
+      const int64_t o = static_cast<int64_t>(unit) * a.L + kt;
+      float S = (attn + a.alpha * g_in) - a.beta * r_in;
+      if (a.protect_window && kt >= m.L - a.w) S = INFINITY;
+      sc.attn[o] = attn;
+      sc.score[o] = S;
+      if (a.dbg_attn) a.dbg_attn[dbase + kt] = attn;
+      if (a.dbg_score) a.dbg_score[dbase + kt] = S;
+    }
+    // every TMEM read of D2 precedes the next chunk's MMA
+    tc_fence_before();
+    __syncthreads();
   }
   if (fail && tid == 0) record_error(a.err, ZP_ERR_TIMEOUT);
+  if (tid == 0 && tma_pending) mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
@@ -500,6 +585,7 @@ zp_status launch_compress_long(const CUtensorMap& tmK, const CUtensorMap& tmQ, c
   const int64_t units = static_cast<int64_t>(a.R) * a.nl * a.Hkv;
   LongScratch sc{};
   sc.nch = (a.L + kKeysPerCta - 1) / kKeysPerCta;
+  sc.ngrp = (sc.nch + kChunksPerCta - 1) / kChunksPerCta;
   uint8_t* p = static_cast<uint8_t*>(scratch);
   sc.part = reinterpret_cast<float2*>(p);
   p += static_cast<size_t>(units) * sc.nch * kRows * sizeof(float2);
@@ -520,7 +606,7 @@ zp_status launch_compress_long(const CUtensorMap& tmK, const CUtensorMap& tmQ, c
       attr = cudaFuncSetAttribute(long_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   });
   if (attr != cudaSuccess) return ZP_ERR_CUDA;
-  const unsigned chunks = static_cast<unsigned>(units * sc.nch);
+  const unsigned chunks = static_cast<unsigned>(units * sc.ngrp);
   long_stats_kernel<<<chunks, kThreads, smem, st>>>(tmK, tmQ, a, sc);
   long_score_kernel<<<chunks, kThreads, smem, st>>>(tmK, tmQ, a, sc);
   long_select_kernel<<<static_cast<unsigned>(units), kSelThreads, 0, st>>>(a, sc);
