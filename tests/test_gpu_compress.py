@@ -157,6 +157,20 @@ def test_eviction_counts_at_the_path_boundaries(zp):
     assert _check_all(zp, wl, mutate=mutate) == 0
 
 
+def test_maximum_length_multipass(zp):
+    # the longest sequences the library takes (L = 16384, the multi-pass form): a decode trigger
+    # (E = 16) and, through a per-request budget of 64 blocks, a prefill-sized eviction
+    # (E = 16384 - 1008 = 15376) in the same launch
+    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                             n_max=1024)
+
+    def mutate(inp):
+        assert (inp.seq_len[:2] == 16384).all()
+        inp.n_max_req = np.array([1024, 64], dtype=np.int32)
+
+    assert _check_all(zp, wl, mutate=mutate) <= 2
+
+
 def test_bad_block_id_skips_the_request_and_reports(zp):
     wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, n_max=16)
     zipage, runner = zp
@@ -182,7 +196,7 @@ def test_unsupported_and_empty_calls(zp):
     wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=1, num_layers=1, n_max=8)
     inp = synth.make_inputs(wl, "cpu")
     batch = runner.CompressionBatch(inp, "cuda")
-    with pytest.raises(zipage.ZipageError) as e:   # L = 160*16 > 2048 keys per unit
+    with pytest.raises(zipage.ZipageError) as e:   # n_max = 160 is wider than the 8-entry tables
         zipage.zp_compress(batch.pool, batch.d_tables, batch.d_seq, batch.d_qslot, batch.d_dst,
                            batch.obs_q, batch.gs, dict(batch.params, n_max=160), batch.workspace)
     assert e.value.status in (zipage.ZP_ERR_UNSUPPORTED, zipage.ZP_ERR_INVALID_ARG)
