@@ -8,12 +8,15 @@
 //   R_all[t] = (1 / (L-1)) * sum_{j < L, j != t} cos(k_t, k_j),   cos with norms clamped at 1e-12,
 // and 0 for L < 2 and for t >= L (up to the row length of the output).
 //
-// GB300 mapping.  One CTA per (unit, 128-row tile of t), 128 threads.  The CTA TMA-loads its 128
-// key rows once (A, 128-byte swizzle, one 3-D box per (block, 64-column half)) and streams the
-// unit's key tiles (B) through a two-stage ring.  tcgen05 MMA computes each 128 x 128 Gram tile
-// A B^T into one of two TMEM accumulators while the four warps reduce the previous one: thread =
-// row t (TMEM lane) adds Gram[t][j] / |k_j| over the tile's 128 columns.  The similarity matrix
-// is never stored.  R_all[t] = (acc / |k_t| - cos(k_t, k_t)) / (L-1).  All waits are bounded.
+// GB300 mapping.  One CTA per (unit, pair of 128-row tiles of t), one CTA per SM, warp-
+// specialised: a producer warp TMA-loads the CTA's 256 key rows once (A, 128-byte swizzle, one
+// 3-D box per (block, 64-column half)) and streams the unit's 128-key tiles (B) through a
+// four-stage ring; an MMA warp issues the two 128 x 128 Gram tiles A_h B^T of each key tile on
+// tcgen05 into one of two TMEM buffers; eight epilogue warps (thread = row t) add Gram[t][j] / |k_j|
+// over the tile's columns while the next tile is multiplied.  Stages and buffers are handed over
+// with mbarriers (full / empty, TMEM full / empty), so copies, MMAs and reductions overlap.  The
+// similarity matrix is never stored.  R_all[t] = (acc / |k_t| - cos(k_t, k_t)) / (L-1).  Every
+// wait is bounded; a role that gives up raises a flag that ends the others' waits too.
 #include <algorithm>
 #include <mutex>
 
@@ -24,9 +27,14 @@ namespace zp {
 namespace {
 
 constexpr int kTile = 128;        // rows per tile = TMEM lanes = MMA M and N
-constexpr int kThreadsA = 128;    // thread = row of the CTA's tile
-constexpr uint32_t kColsA = 256;  // two 128-column fp32 accumulators
+constexpr int kThreadsA = 128;    // pre-pass: thread = key
+constexpr int kEpiWarps = 8;      // epilogue warps: thread = row of the CTA's two row tiles
+constexpr int kProdWarp = 8, kMmaWarp = 9;
+constexpr int kThreadsW = 320;    // 8 epilogue warps + producer warp + MMA warp
+constexpr int kStages = 4;        // B ring depth
+constexpr uint32_t kColsA = 512;  // [row half h][buffer u] 128-column fp32 accumulators
 constexpr int kMaxTabA = 256;     // block-table entries per request (L <= 4096 at b = 16)
+constexpr int kMaxLA = kMaxTabA * 16;
 constexpr uint64_t kWaitNsA = 2000000000ull;
 
 struct ApArgs {
@@ -41,36 +49,56 @@ struct ApArgs {
 };
 
 struct __align__(1024) ApSmem {
-  uint8_t A[2][kTile * 128];     // [d-half][row][128 B], 128-byte swizzle: this CTA's rows
-  uint8_t B[2][2][kTile * 128];  // [stage][d-half][row][128 B]: the streamed key tiles
-  float inv_b[2][kTile];         // reciprocal norms of each stage's rows
+  uint8_t A[2][2][kTile * 128];         // [row half][d-half][row][128 B], 128-byte swizzle: the CTA's rows
+  uint8_t B[kStages][2][kTile * 128];   // [stage][d-half][row][128 B]: the streamed key tiles
+  float inv[kMaxLA];                    // reciprocal key norms of the unit
   int tab[kMaxTabA];
-  uint64_t bar_a, bar_b[2], bar_mma[2];
+  uint64_t bar_a, full[kStages], empty[kStages], tfull[2], tempty[2];
   uint32_t tmem_base;
+  int abort;                            // a role gave up a wait: the others stop waiting
 };
 
 __device__ __forceinline__ void ap_record_error(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-// Zeroes row `row` of a swizzled tile (rows past the sequence must not contribute).
-__device__ __forceinline__ void zero_row(uint8_t (&T)[2][kTile * 128], int row, int nhalf) {
-  for (int hd = 0; hd < nhalf; ++hd)
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) *reinterpret_cast<uint4*>(&T[hd][row * 128 + ch * 16]) = make_uint4(0, 0, 0, 0);
+// Issues the TMA of the 128 key rows [row0, row0 + 128) of the unit into `dst`, only for blocks
+// that hold tokens of the sequence, and registers their bytes on `bar` (rows past the
+// sequence keep whatever the buffer held; their columns and rows are never used).  Called by a
+// whole warp: lane 0 registers the bytes, then lane bi issues the boxes of block bi (one TMA
+// instruction stream per lane instead of one thread issuing every box).
+__device__ __forceinline__ void load_rows(uint8_t (&dst)[2][kTile * 128], const CUtensorMap* tm, uint64_t* bar,
+                                          const ApArgs& a, const int* tab, int layer, int h, int row0, int L,
+                                          int lane) {
+  const int nhalf = a.d / 64;
+  const int blk0 = row0 >> a.b_shift;
+  const int nblk = max(0, min(kTile >> a.b_shift, ((L + a.b - 1) >> a.b_shift) - blk0));
+  if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nblk * a.b * a.d * 2));
+  __syncwarp();
+  if (lane < nblk)  // nblk <= 128 / 16 = 8
+    for (int hd = 0; hd < nhalf; ++hd)
+      tma_load_3d(&dst[hd][lane * a.b * 128], tm, bar, hd * 64, h * a.b, layer * a.num_blocks + tab[blk0 + lane]);
+  __syncwarp();
 }
 
-// Issues the TMA of key tile `tile` (rows [128*tile, 128*tile + 128) of the unit) into `dst`,
-// only for blocks that hold tokens of the sequence; returns the bytes registered on `bar`.
-__device__ __forceinline__ void load_tile(uint8_t (&dst)[2][kTile * 128], const CUtensorMap* tm, uint64_t* bar,
-                                          const ApArgs& a, const int* tab, int layer, int h, int tile, int L) {
-  const int nhalf = a.d / 64;
-  const int blk0 = (tile * kTile) >> a.b_shift;
-  const int nblk = min(kTile >> a.b_shift, ((L + a.b - 1) >> a.b_shift) - blk0);
-  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nblk * a.b * a.d * 2));
-  for (int bi = 0; bi < nblk; ++bi)
-    for (int hd = 0; hd < nhalf; ++hd)
-      tma_load_3d(&dst[hd][bi * a.b * 128], tm, bar, hd * 64, h * a.b, layer * a.num_blocks + tab[blk0 + bi]);
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Waits for phase `parity` of `bar`; gives up (false) after the time limit, or at once when
+// another role has given up.  A thread that gives up raises the flag.
+__device__ __forceinline__ bool ap_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitNsA) {
+      *abort = 1;
+      return false;
+    }
+  }
 }
 
 // Pre-pass: the squared norm of every key of every unit (t < L; 0 past it), in fp32, read once
@@ -104,38 +132,47 @@ __global__ void __launch_bounds__(kThreadsA) key_sq_norm_kernel(const ApArgs a) 
   a.sq[static_cast<int64_t>(unit) * a.L + t] = acc;
 }
 
-__global__ void __launch_bounds__(kThreadsA, 2)
+__global__ void __launch_bounds__(kThreadsW, 1)
     all_pairs_redundancy_kernel(const __grid_constant__ CUtensorMap tmK, const ApArgs a) {
   extern __shared__ uint8_t smem_raw[];
   ApSmem& s = *reinterpret_cast<ApSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int unit = static_cast<int>(blockIdx.x) / a.nt, it = static_cast<int>(blockIdx.x) % a.nt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int np = (a.nt + 1) / 2;  // row-tile pairs per unit
+  const int unit = static_cast<int>(blockIdx.x) / np, ip = static_cast<int>(blockIdx.x) % np;
   const int h = unit % a.Hkv, layer = (unit / a.Hkv) % a.layers, r = unit / a.Hkv / a.layers;
-  const int nhalf = a.d / 64;
-  const int t = it * kTile + tid;  // this thread's row
+  const int row0 = ip * 2 * kTile;  // first row of the pair
   float* const out = a.out + static_cast<int64_t>(unit) * a.L;
   const int L = a.seq_len[r];
   if (L < 0 || L > a.L) {
-    if (tid == 0 && it == 0) ap_record_error(a.err, ZP_ERR_BAD_TABLE);
+    if (tid == 0 && ip == 0) ap_record_error(a.err, ZP_ERR_BAD_TABLE);
     return;
   }
-  // rows of this tile past the sequence (or all of them) are 0
-  if (t < a.L && (t >= L || L < 2)) out[t] = 0.0f;
-  if (it * kTile >= L || L < 2) return;
+  // rows of this pair past the sequence (or all of them) are 0
+  for (int t = row0 + tid; t < min(row0 + 2 * kTile, a.L); t += kThreadsW)
+    if (t >= L || L < 2) out[t] = 0.0f;
+  if (row0 >= L || L < 2) return;
 
   const int nblk = (L + a.b - 1) >> a.b_shift;
   bool bad = false;
-  for (int i = tid; i < nblk; i += kThreadsA) {
+  for (int i = tid; i < nblk; i += kThreadsW) {
     const int e = a.block_tables[static_cast<int64_t>(r) * a.max_blocks + i];
     s.tab[i] = e;
     bad |= (e < 0 || e >= a.num_blocks);
   }
+  const int ntc = (L + kTile - 1) / kTile;  // key tiles of the unit
+  const float* const sq_unit = a.sq + static_cast<int64_t>(unit) * a.L;
+  const bool half1 = row0 + kTile < L;  // the second row tile holds rows of the sequence
   if (tid == 0) {
-    mbar_init(&s.bar_a, 1);
-    mbar_init(&s.bar_b[0], 1);
-    mbar_init(&s.bar_b[1], 1);
-    mbar_init(&s.bar_mma[0], 1);
-    mbar_init(&s.bar_mma[1], 1);
+    mbar_init(&s.bar_a, half1 ? 2 : 1);  // one arrival (with its bytes) per loaded row tile
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], 1);
+    }
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&s.tfull[u], 1);
+      mbar_init(&s.tempty[u], kEpiWarps);
+    }
+    s.abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmK);
   }
@@ -144,132 +181,133 @@ __global__ void __launch_bounds__(kThreadsA, 2)
     return;
   }
   if (warp == 0) tmem_alloc(&s.tmem_base, kColsA);
-  const int ntc = (L + kTile - 1) / kTile;  // key tiles of the unit
-  // (tid 0) mbarrier phases and copies/MMAs in flight, one bit each: bit st for bar_b[st],
-  // bit 2 + u for bar_mma[u], bit 4 for bar_a
-  uint32_t ph = 0, pend = 0;
-  bool ok = true;  // (tid 0)
-  if (tid == 0) {
-    load_tile(s.A, &tmK, &s.bar_a, a, s.tab, layer, h, it, L);
-    pend |= 16u;
-    for (int st = 0; st < 2 && st < ntc; ++st) {
-      load_tile(s.B[st], &tmK, &s.bar_b[st], a, s.tab, layer, h, st, L);
-      pend |= 1u << st;
-    }
-    ok = mbar_wait_bounded(&s.bar_a, 0, kWaitNsA);
-    if (ok) pend &= ~16u;
-  }
   tc_fence_before();
-  bool fail = __syncthreads_or(!ok);
+  __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  float inv_a = 0.0f, self = 0.0f;
-  const float* const sq_unit = a.sq + static_cast<int64_t>(unit) * a.L;
-  if (!fail) {
-    if (t >= L) zero_row(s.A, tid, nhalf);
-    const float sq = t < L ? sq_unit[t] : 0.0f;
-    inv_a = 1.0f / fmaxf(sqrtf(sq), 1e-12f);
-    self = sq * inv_a * inv_a;  // cos(k_t, k_t): 1, or 0 for a zero key
-  }
-  fence_proxy_async_smem();
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const uint32_t idesc = idesc_bf16_f32(kTile, kTile);
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  volatile int* const abort = &s.abort;
 
-  // Reduces the accumulator of key tile j into acc (thread = row).
-  auto epilogue = [&](int j) {
-    const int u = j & 1;
-    if (tid == 0) {
-      const bool w = mbar_wait_bounded(&s.bar_mma[u], (ph >> (2 + u)) & 1u, kWaitNsA);
-      if (w) {
-        ph ^= 4u << u;
-        pend &= ~(4u << u);
-      }
-      ok = ok && w;
+  if (warp == kProdWarp) {
+    // A: the pair's rows; then the key tiles through the ring (the whole warp: lane 0 waits and
+    // registers bytes, every lane issues the boxes of one block)
+    load_rows(s.A[0], &tmK, &s.bar_a, a, s.tab, layer, h, row0, L, lane);
+    if (half1) load_rows(s.A[1], &tmK, &s.bar_a, a, s.tab, layer, h, row0 + kTile, L, lane);
+    int last = -1;  // the last key tile issued
+    for (int jt = 0; jt < ntc; ++jt) {
+      const int st = jt % kStages;
+      bool go = true;
+      if (lane == 0 && jt >= kStages) go = ap_wait(&s.empty[st], ((jt / kStages) - 1) & 1, abort);
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      load_rows(s.B[st], &tmK, &s.full[st], a, s.tab, layer, h, jt * kTile, L, lane);
+      last = jt;
     }
-    tc_fence_before();
-    fail |= __syncthreads_or(!ok);
-    tc_fence_after();
-    if (fail) return;
-#pragma unroll 1
-    for (int c4 = 0; c4 < 4; ++c4) {
-      uint32_t v[32];
-      tmem_ld32_issue(tbase + lane_base + u * kTile + c4 * 32, v);
-      tmem_wait_ld(v);
-      const float4* ib = reinterpret_cast<const float4*>(&s.inv_b[u][c4 * 32]);
+    // copies still in flight after a give-up land before the shared memory is released
+    if (lane == 0) {
+      if (*abort)
+        for (int jt = max(0, last - kStages + 1); jt <= last; ++jt)
+          mbar_wait_bounded(&s.full[jt % kStages], (jt / kStages) & 1, kWaitNsA);
+      mbar_wait_bounded(&s.bar_a, 0, kWaitNsA);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTile, kTile);
+      int issued = 0;
+      if (ap_wait(&s.bar_a, 0, abort)) {
+        for (int jt = 0; jt < ntc; ++jt) {
+          const int st = jt % kStages, u = jt & 1;
+          if (!ap_wait(&s.full[st], (jt / kStages) & 1, abort)) break;
+          if (jt >= 2 && !ap_wait(&s.tempty[u], ((jt >> 1) - 1) & 1, abort)) break;
+          tc_fence_after();
+          for (int hh = 0; hh < (half1 ? 2 : 1); ++hh)
+            for (int kk = 0; kk < a.d / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(smem_u32(&s.A[hh][kk >> 2][(kk & 3) * 32]));
+              const uint64_t bd = smem_desc_sw128(smem_u32(&s.B[st][kk >> 2][(kk & 3) * 32]));
+              mma_bf16(tbase + hh * 2 * kTile + u * kTile, ad, bd, idesc, kk > 0);
+            }
+          mma_commit(&s.empty[st]);  // the stage is free once these MMAs have read it
+          mma_commit(&s.tfull[u]);
+          issued = jt + 1;
+        }
+      }
+      // MMAs still in flight after a give-up complete before TMEM is released
+      if (*abort && issued > 0) mbar_wait_bounded(&s.tfull[(issued - 1) & 1], ((issued - 1) >> 1) & 1, kWaitNsA);
+    }
+  } else {
+    // epilogue: the reciprocal norms of the unit's keys first (while the first copies and MMAs
+    // run), then warp w reads TMEM lanes 32 (w % 4) .. + 31 of row half w / 4
+    constexpr int kEpi = kEpiWarps * 32;
+    for (int i0 = 0; i0 < ntc * kTile; i0 += 4 * kEpi) {
+      float sqv[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 w = ib[q];
-        acc[0] = fmaf(__uint_as_float(v[4 * q + 0]), w.x, acc[0]);
-        acc[1] = fmaf(__uint_as_float(v[4 * q + 1]), w.y, acc[1]);
-        acc[2] = fmaf(__uint_as_float(v[4 * q + 2]), w.z, acc[2]);
-        acc[3] = fmaf(__uint_as_float(v[4 * q + 3]), w.w, acc[3]);
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + e * kEpi + tid;
+        sqv[e] = (i < L) ? sq_unit[i] : 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + e * kEpi + tid;
+        if (i < ntc * kTile) s.inv[i] = i < L ? 1.0f / fmaxf(sqrtf(sqv[e]), 1e-12f) : 0.0f;
       }
     }
-  };
-
-  for (int jt = 0; jt < ntc && !fail; ++jt) {
-    const int st = jt & 1;
-    if (tid == 0) {
-      const bool w = mbar_wait_bounded(&s.bar_b[st], (ph >> st) & 1u, kWaitNsA);
-      if (w) {
-        ph ^= 1u << st;
-        pend &= ~(1u << st);
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");  // the epilogue warps only
+    const int hh = warp >> 2, q = warp & 3;
+    const int t = row0 + hh * kTile + q * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int jt = 0; jt < ntc; ++jt) {
+      const int u = jt & 1;
+      if (!ap_wait(&s.tfull[u], (jt >> 1) & 1, abort)) break;
+      tc_fence_after();
+      const int nvalid = min(kTile, L - jt * kTile);  // columns of keys of the sequence
+      const float* const ib = &s.inv[jt * kTile];
+      uint32_t v4[4][32];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32_issue(tbase + lane_base + hh * 2 * kTile + u * kTile + c4 * 32, v4[c4]);
+      tmem_wait_ld(v4[0]);
+      tmem_ld_dep(v4[1]);
+      tmem_ld_dep(v4[2]);
+      tmem_ld_dep(v4[3]);
+      // the accumulator buffer is free as soon as it has been read
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[u]);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const uint32_t (&v)[32] = v4[c4];
+        const float4* ib4 = reinterpret_cast<const float4*>(ib + c4 * 32);
+        if (c4 * 32 + 32 <= nvalid) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 w = ib4[e];
+            acc[0] = fmaf(__uint_as_float(v[4 * e + 0]), w.x, acc[0]);
+            acc[1] = fmaf(__uint_as_float(v[4 * e + 1]), w.y, acc[1]);
+            acc[2] = fmaf(__uint_as_float(v[4 * e + 2]), w.z, acc[2]);
+            acc[3] = fmaf(__uint_as_float(v[4 * e + 3]), w.w, acc[3]);
+          }
+        } else {
+          // the columns past the sequence may hold anything (the tail of the last block, or
+          // an earlier tile): they are skipped, not multiplied by zero
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c4 * 32 + j < nvalid) acc[j & 3] = fmaf(__uint_as_float(v[j]), ib[c4 * 32 + j], acc[j & 3]);
+        }
       }
-      ok = ok && w;
     }
-    fail |= __syncthreads_or(!ok);
-    if (fail) break;
-    const int tj = jt * kTile + tid;  // the key row this thread normalises
-    if (tj >= L) zero_row(s.B[st], tid, nhalf);
-    s.inv_b[st][tid] = tj < L ? 1.0f / fmaxf(sqrtf(sq_unit[tj]), 1e-12f) : 0.0f;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      for (int kk = 0; kk < a.d / 16; ++kk) {
-        const uint64_t ad = smem_desc_sw128(smem_u32(&s.A[kk >> 2][(kk & 3) * 32]));
-        const uint64_t bd = smem_desc_sw128(smem_u32(&s.B[st][kk >> 2][(kk & 3) * 32]));
-        mma_bf16(tbase + st * kTile, ad, bd, idesc, kk > 0);
-      }
-      mma_commit(&s.bar_mma[st]);
-      pend |= 4u << st;
-    }
-    if (jt >= 1) {
-      epilogue(jt - 1);
-      if (fail) break;
-      // stage (jt + 1) & 1 == (jt - 1) & 1 is free: its MMA has completed and its norms are read
-      __syncthreads();
-      if (tid == 0 && jt + 1 < ntc) {
-        load_tile(s.B[(jt + 1) & 1], &tmK, &s.bar_b[(jt + 1) & 1], a, s.tab, layer, h, jt + 1, L);
-        pend |= 1u << ((jt + 1) & 1);
-      }
-    }
-  }
-  if (!fail) epilogue(ntc - 1);
-  if (!fail && t < L) {
-    const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-    out[t] = (sum * inv_a - self) / static_cast<float>(L - 1);
-  }
-  if (fail && tid == 0) ap_record_error(a.err, ZP_ERR_TIMEOUT);
-  // copies and MMAs still in flight after a failed wait: wait for them (bounded) before the
-  // shared memory and TMEM are released
-  if (tid == 0) {
-    if (pend & 16u) mbar_wait_bounded(&s.bar_a, 0, kWaitNsA);
-    for (int st = 0; st < 2; ++st) {
-      if (pend & (1u << st)) mbar_wait_bounded(&s.bar_b[st], (ph >> st) & 1u, kWaitNsA);
-      if (pend & (4u << st)) mbar_wait_bounded(&s.bar_mma[st], (ph >> (2 + st)) & 1u, kWaitNsA);
+    if (!*abort && t < L) {
+      const float sq = sq_unit[t];
+      const float inv_a = s.inv[t];
+      const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      out[t] = (sum * inv_a - sq * inv_a * inv_a) / static_cast<float>(L - 1);
     }
   }
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
+  if (tid == 0 && s.abort) ap_record_error(a.err, ZP_ERR_TIMEOUT);
   if (warp == 0) tmem_dealloc(tbase, kColsA);
 }
 
-// two CTAs per SM (228 KB of shared memory per SM, 1 KB reserved per CTA, 1 KB alignment slack)
-static_assert(sizeof(ApSmem) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "shared memory must allow two CTAs per SM");
+// one CTA per SM: 227 KB of shared memory per CTA at most, 1 KB alignment slack
+static_assert(sizeof(ApSmem) + 1024 <= 227 * 1024, "shared memory of one CTA");
 
 }  // namespace
 }  // namespace zp
@@ -304,7 +342,8 @@ extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32
   if (!aligned(pool->base, 16)) return ZP_ERR_INVALID_ARG;
   if (static_cast<int64_t>(layers) * pool->num_blocks >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
   const int nt = (L + kTile - 1) / kTile;
-  const int64_t ctas = static_cast<int64_t>(R) * layers * Hkv * nt;
+  const int64_t ctas = static_cast<int64_t>(R) * layers * Hkv * nt;          // pre-pass
+  const int64_t pairs = static_cast<int64_t>(R) * layers * Hkv * ((nt + 1) / 2);  // main kernel
   if (ctas >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -344,6 +383,6 @@ extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32
   });
   if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
   key_sq_norm_kernel<<<static_cast<unsigned>(ctas), kThreadsA, 0, st>>>(a);
-  all_pairs_redundancy_kernel<<<static_cast<unsigned>(ctas), kThreadsA, smem, st>>>(tmK, a);
+  all_pairs_redundancy_kernel<<<static_cast<unsigned>(pairs), kThreadsW, smem, st>>>(tmK, a);
   return cudaGetLastError() == cudaSuccess ? ZP_OK : ZP_ERR_CUDA;
 }
