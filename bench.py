@@ -467,9 +467,19 @@ def run_mixed(args):
     from paged_kv_cache_obs_gb300 import runner, synth, zipage
     torch.cuda.set_device(0)
     wl = workload_of(args)
+    # the pool of the mixed configuration: 120k blocks of 2 MiB (all layers), as many as fit
+    # beside the rest of the step with a margin
+    per_block = wl.num_layers * 2 * wl.num_kv_heads * wl.block_size * wl.head_dim * 2
+    free, _ = torch.cuda.mem_get_info()
+    nb = min(args.pool_blocks, int((free - (24 << 30)) // per_block))
+    if nb > 0:
+        wl = wl.scaled(pool_blocks=nb)
     inp = synth.make_inputs(wl, "cuda")
     R = inp.num_compress
-    pristine = inp.pool.clone()
+    # only the compressing requests' blocks change: they alone are restored between steps
+    comp_ids = torch.as_tensor(np.unique(inp.block_tables[:R][inp.block_tables[:R] >= 0]), dtype=torch.int64,
+                               device="cuda")
+    pristine = inp.pool.index_select(1, comp_ids)
     gs0 = inp.global_scores.clone()
     batch = runner.CompressionBatch(inp, "cuda", pool=inp.pool)
     p = wl.params()
@@ -489,7 +499,7 @@ def run_mixed(args):
                                         stream=main)
 
     def timed(fn_c, fn_d):
-        batch.pool.copy_(pristine)
+        batch.pool.index_copy_(1, comp_ids, pristine)
         batch.gs.copy_(gs0)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -641,6 +651,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--requests", type=int, default=0, help="override the workload's request count (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
+    ap.add_argument("--pool-blocks", type=int, default=120000,
+                    help="mixed workload: pool size in blocks (capped by free device memory; 0 = just enough)")
     ap.add_argument("--ablation", choices=["all_pairs"], default=None,
                     help="time the original all-pairs redundancy against the fused Lightning pass")
     args = ap.parse_args(argv)

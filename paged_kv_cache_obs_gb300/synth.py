@@ -194,25 +194,40 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
     phys_pos = phys_pos.to(dev)
 
     # ---- KV pool, one layer at a time ---------------------------------------------------
-    pool = torch.zeros((nl, NB, 2, Hkv, b, d), dtype=torch.bfloat16, device=dev)
+    # A pool far larger than the blocks in use (the mixed workload's 120k blocks) is left
+    # uninitialised except for the referenced blocks: the kernels read only blocks of some
+    # table (a target block is written before it is read).  Otherwise every block is drawn.
+    sparse = NB > 4 * (needed + targets)
+    if sparse:
+        pool = torch.empty((nl, NB, 2, Hkv, b, d), dtype=torch.bfloat16, device=dev)
+        ids = torch.as_tensor(np.nonzero(refcount)[0], dtype=torch.int64, device=dev)
+    else:
+        pool = torch.zeros((nl, NB, 2, Hkv, b, d), dtype=torch.bfloat16, device=dev)
+        ids = None
+    nfill = NB if ids is None else int(ids.numel())
+    fpos = phys_pos if ids is None else phys_pos[ids]
     for l in range(nl):
         if wl.key_recipe == "clustered":
             cent = torch.randn((Hkv, 64, d), generator=g, device=dev)
-            pick = torch.randint(0, 64, (NB, Hkv, 2), generator=g, device=dev)
-            which = torch.randint(0, 2, (NB, Hkv, b), generator=g, device=dev)
-            cid = torch.gather(pick, 2, which)  # [NB, Hkv, b] centroid of each token
+            pick = torch.randint(0, 64, (nfill, Hkv, 2), generator=g, device=dev)
+            which = torch.randint(0, 2, (nfill, Hkv, b), generator=g, device=dev)
+            cid = torch.gather(pick, 2, which)  # [blocks, Hkv, b] centroid of each token
             hidx = torch.arange(Hkv, device=dev)[None, :, None].expand_as(cid)
-            k = cent[hidx, cid] + 0.05 * torch.randn((NB, Hkv, b, d), generator=g, device=dev)
-            heavy = torch.rand((NB, Hkv, b), generator=g, device=dev) < 0.10
+            k = cent[hidx, cid] + 0.05 * torch.randn((nfill, Hkv, b, d), generator=g, device=dev)
+            heavy = torch.rand((nfill, Hkv, b), generator=g, device=dev) < 0.10
             k = torch.where(heavy[..., None], 4.0 * k, k)
         else:
-            k = torch.randn((NB, Hkv, b, d), generator=g, device=dev)
+            k = torch.randn((nfill, Hkv, b, d), generator=g, device=dev)
             if wl.key_recipe == "rope":
-                pos = phys_pos.clamp(min=0)[:, None, None] * b + torch.arange(b, device=dev)[None, None, :]
-                k = _rope_(k, pos.expand(NB, Hkv, b), wl.rope_theta)
-        v = torch.randn((NB, Hkv, b, d), generator=g, device=dev)
-        pool[l, :, 0] = k.to(torch.bfloat16)
-        pool[l, :, 1] = v.to(torch.bfloat16)
+                pos = fpos.clamp(min=0)[:, None, None] * b + torch.arange(b, device=dev)[None, None, :]
+                k = _rope_(k, pos.expand(nfill, Hkv, b), wl.rope_theta)
+        v = torch.randn((nfill, Hkv, b, d), generator=g, device=dev)
+        if ids is None:
+            pool[l, :, 0] = k.to(torch.bfloat16)
+            pool[l, :, 1] = v.to(torch.bfloat16)
+        else:
+            pool[l].index_copy_(0, ids, torch.stack((k, v), dim=1).to(torch.bfloat16))
+        del k, v
 
     # ---- window queries and carried global scores (one query slot per compressing request)
     M = R
