@@ -194,10 +194,10 @@ def make_inputs(wl: Workload, device="cpu", seed: int | None = None) -> Inputs:
     phys_pos = phys_pos.to(dev)
 
     # ---- KV pool, one layer at a time ---------------------------------------------------
-    # A pool far larger than the blocks in use (the mixed workload's 120k blocks) is left
+    # A requested pool far larger than the blocks in use (the mixed workload's 120k blocks) is left
     # uninitialised except for the referenced blocks: the kernels read only blocks of some
     # table (a target block is written before it is read).  Otherwise every block is drawn.
-    sparse = NB > 4 * (needed + targets)
+    sparse = bool(wl.pool_blocks) and NB > 4 * (needed + targets)
     if sparse:
         pool = torch.empty((nl, NB, 2, Hkv, b, d), dtype=torch.bfloat16, device=dev)
         ids = torch.as_tensor(np.nonzero(refcount)[0], dtype=torch.int64, device=dev)
