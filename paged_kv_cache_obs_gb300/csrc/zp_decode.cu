@@ -256,7 +256,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     }
   }
   __syncthreads();
-  // merge the warps: thread -> (g, dim) pairs
+  // merge the warps: thread -> (g, dim) pairs; a request of one split writes its output here,
+  // longer ones write partials for decode_combine_kernel
+  const bool single = nblk <= kBlocksPerSplit;
   for (int idx = tid; idx < G * D; idx += kThreads) {
     const int g = idx / D, dim = idx % D;
     float M = -INFINITY;
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         As += sm_acc[ww][g][dim] * cw;
       }
     const int qh = h * G + g;
-    if (a.max_splits == 1) {
+    if (single) {
       a.out[(static_cast<int64_t>(r) * a.Hq + qh) * D + dim] = f2bf16(Ls > 0.0f ? As / Ls : 0.0f);
     } else {
       float* p = a.part + ((static_cast<int64_t>(r) * a.Hq + qh) * a.max_splits + split) * (D + 2);
@@ -294,6 +296,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
   if (seq < 1 || seq > a.max_blocks * a.b) return;
   const int nblk = (seq + a.b - 1) / a.b;
   const int ns = (nblk + kBlocksPerSplit - 1) / kBlocksPerSplit;
+  if (ns == 1) return;  // written by the decode kernel itself
   const float* p = a.part + (static_cast<int64_t>(r) * a.Hq + qh) * a.max_splits * (D + 2);
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, p[s * (D + 2) + D]);
