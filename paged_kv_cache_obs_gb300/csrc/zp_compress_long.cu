@@ -8,7 +8,7 @@
 //               Lightning redundancy of the chunk's keys (warp-level MMA);
 //   2. score:   per chunk: every row's normaliser from all chunks' partials, K again, D2 =
 //               K Q^T, the attention mass of each key and S = attn + a*G - b*R;
-//               (a CTA of these two kernels takes up to eight consecutive chunks of one unit and
+//               (a CTA of these two kernels takes up to 16 consecutive chunks of one unit and
 //               copies each chunk's K while the previous chunk's TMEM pass runs)
 //   3. select:  per unit: the E = L - k lowest eviction keys by an 8-pass radix select of the
 //               64-bit keys (order(S), ~t), destinations by a block-wide scan, and the global
@@ -71,7 +71,7 @@ __device__ __forceinline__ UnitMeta unit_meta(const CompressArgs& a, int unit) {
 // A CTA of the stats and score kernels takes a group of up to kChunksPerCta consecutive chunks
 // of one unit: the window queries, the mbarriers, TMEM and the block ids load once, and each
 // chunk's K is copied while the previous chunk's TMEM pass runs.
-constexpr int kChunksPerCta = 8;
+constexpr int kChunksPerCta = 16;
 constexpr int kGroupBlocks = kChunksPerCta * kKeysPerCta / 16;  // block ids of a group (b >= 16)
 
 // TMA of one chunk's K blocks (tid 0); the first chunk of a CTA also brings the window queries.
