@@ -2,6 +2,7 @@
 test read them), another seed gives other bytes, and the workloads have the shapes and
 structure their recipes state."""
 import numpy as np
+import torch
 
 from paged_kv_cache_obs_gb300 import synth
 
@@ -35,3 +36,18 @@ def test_workload_structure():
     # block ids of different requests are otherwise disjoint
     own = [set(inp.block_tables[r, 16:wl.n_max].tolist()) for r in range(3)]
     assert not (own[0] & own[1]) and not (own[1] & own[2])
+
+
+def test_large_requested_pool_draws_the_referenced_blocks():
+    # the mixed workload's pool is far larger than the blocks in use: only the blocks of some
+    # table are drawn, with the same recipe, and the ids spread over the whole pool
+    wl = synth.WORKLOADS["mixed"].scaled(num_requests=2, num_layers=2, num_decode=3, pool_blocks=4000)
+    inp = synth.make_inputs(wl, "cpu")
+    assert inp.pool.shape[1] == 4000
+    used = np.unique(inp.block_tables[inp.block_tables >= 0])
+    assert (inp.refcount[used] >= 1).all()
+    assert used.max() > 1000  # a permutation of the whole pool, not of its first blocks
+    k = inp.pool[:, torch.as_tensor(used), 0].float()
+    v = inp.pool[:, torch.as_tensor(used), 1].float()
+    assert torch.isfinite(k).all() and torch.isfinite(v).all()
+    assert float(v.std()) > 0.5 and float(k.abs().mean()) > 0.1
