@@ -13,9 +13,9 @@
 //   3. select:  per unit: the E = L - k lowest eviction keys by an 8-pass radix select of the
 //               64-bit keys (order(S), ~t), destinations by a block-wide scan, and the global
 //               scores updated in place (every read before any write);
-//   4. compact: per unit: the moved K and V rows, 128 destination slots at a time in
+//   4. compact: per unit: the moved K and V rows, 32 destination slots at a time in
 //               increasing order (dst <= src, so a chunk's rows are read before anything lands
-//               on them).
+//               on them), the next chunk's loads in flight while a chunk is written.
 // Every wait is bounded.  A unit with bad metadata or block ids is reported and left untouched.
 #include <algorithm>
 #include <mutex>
@@ -27,7 +27,6 @@ namespace {
 
 constexpr int kMaxLongL = 16384;
 constexpr int kSelThreads = 1024;
-constexpr int kCompactRows = 128;
 
 struct LongScratch {
   float2* part;  // [units][nch][kRows] (max, exp-sum) of each window row over each chunk
@@ -497,16 +496,19 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   for (int t = m.k_r + tid; t < L; t += kSelThreads) G[t] = 0.0f;  // slots past the k survivors
 }
 
-// 4. In-place compaction of the moved K and V rows, one CTA per unit, 128 destination slots at a
-//    time.  A row only moves to a lower slot (dst <= src), so the sources of the slots past a
+// 4. In-place compaction of the moved K and V rows, one CTA per unit, 32 destination slots at a
+//    time (small chunks keep the registers low enough for four CTAs per SM).  A row only moves to a lower slot (dst <= src), so the sources of the slots past a
 //    chunk all lie past that chunk: chunk by chunk in increasing order, with every read of a
-//    chunk before any of its writes, is a safe order, and every chunk is full of kept rows.  A
-//    chunk's 16-byte pieces are all loaded into registers at once (one memory round trip per
-//    chunk), and the next chunk's per-row byte offsets (source and destination, or -1 for a
-//    row that stays) are computed while those loads are in flight, into a ring of three offset
-//    buffers (a buffer is refilled only after the barrier that follows the writes that used it).
-__global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressArgs a, const LongScratch sc) {
-  __shared__ long long src_off[3][kCompactRows], dst_off[3][kCompactRows];
+//    chunk before any of its writes, is a safe order, and every chunk is full of kept rows.
+//    The loads of chunk c + 1 may run ahead of the writes of chunk c (they read past them), so
+//    the kernel keeps two chunks in registers: while chunk c is written, chunk c + 1 is in
+//    flight.  Per-row byte offsets (source and destination, or -1 for a row that stays) are
+//    computed two chunks ahead into a ring of four buffers (a buffer is refilled only after
+//    the barrier that follows the writes that used it).
+__global__ void __launch_bounds__(kThreads, 4) long_compact_kernel(const CompressArgs a, const LongScratch sc) {
+  constexpr int kRowsC = 32;                                  // destination slots per chunk
+  constexpr int kPerC = kRowsC * 2 * 128 / 8 / kThreads;      // 16-byte pieces per thread at d = 128
+  __shared__ long long src_off[4][kRowsC], dst_off[4][kRowsC];
   const int tid = threadIdx.x;
   const int unit = blockIdx.x;
   const UnitMeta m = unit_meta(a, unit);
@@ -519,10 +521,11 @@ __global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressAr
   const int bm = a.b - 1;
   const int half = a.d / 8;        // 16-byte pieces of a K (or V) row
   const int pieces = 2 * half;     // K then V
-  const int total = kCompactRows * pieces;
-  auto offsets = [&](int j0, int buf) {  // threads 0..127: byte offsets of slot j0 + tid
-    if (tid < kCompactRows) {
-      const int j = j0 + tid;
+  const int total = kRowsC * pieces;
+  const int nchunks = (m.k_r + kRowsC - 1) / kRowsC;
+  auto offsets = [&](int c) {  // threads 0..kRowsC-1: byte offsets of the slots of chunk c
+    if (tid < kRowsC) {
+      const int j = c * kRowsC + tid;
       long long so = -1, dso = -1;
       if (j < m.k_r) {
         const int t = src[j];  // -1 for a reported unit
@@ -534,39 +537,51 @@ __global__ void __launch_bounds__(kThreads) long_compact_kernel(const CompressAr
           }
         }
       }
-      src_off[buf][tid] = so;
-      dst_off[buf][tid] = dso;
+      src_off[c & 3][tid] = so;
+      dst_off[c & 3][tid] = dso;
     }
   };
-  constexpr int kPer = kCompactRows * 2 * 128 / 8 / kThreads;  // pieces per thread at d = 128
-  offsets(0, 0);
-  __syncthreads();
-  int buf = 0;
-  for (int c0 = 0; c0 < m.k_r; c0 += kCompactRows) {
-    uint4 v[kPer];
+  auto load = [&](uint4 (&v)[kPerC], int c) {
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
+    for (int q = 0; q < kPerC; ++q) {
       const int i = tid + q * kThreads;
       v[q] = make_uint4(0u, 0u, 0u, 0u);
       if (i < total) {
         const int row = i / pieces, pc = i % pieces;
-        const long long so = src_off[buf][row];
+        const long long so = src_off[c & 3][row];
         if (so >= 0) v[q] = *reinterpret_cast<const uint4*>(head_base + so + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16);
       }
     }
-    const int nbuf = buf == 2 ? 0 : buf + 1;
-    if (c0 + kCompactRows < m.k_r) offsets(c0 + kCompactRows, nbuf);
-    __syncthreads();  // every read of this chunk precedes every write landing on it
+  };
+  auto store = [&](const uint4 (&v)[kPerC], int c) {
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
+    for (int q = 0; q < kPerC; ++q) {
       const int i = tid + q * kThreads;
       if (i < total) {
         const int row = i / pieces, pc = i % pieces;
-        const long long dso = dst_off[buf][row];
+        const long long dso = dst_off[c & 3][row];
         if (dso >= 0) *reinterpret_cast<uint4*>(head_base + dso + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16) = v[q];
       }
     }
-    buf = nbuf;
+  };
+  if (nchunks == 0) return;
+  offsets(0);
+  if (nchunks > 1) offsets(1);
+  __syncthreads();
+  uint4 va[kPerC], vb[kPerC];
+  load(va, 0);
+  for (int c = 0; c < nchunks; c += 2) {
+    // chunk c is in va
+    if (c + 1 < nchunks) load(vb, c + 1);
+    if (c + 2 < nchunks) offsets(c + 2);
+    __syncthreads();  // every read of chunk c precedes every write landing on it
+    store(va, c);
+    if (c + 1 >= nchunks) break;
+    // chunk c + 1 is in vb
+    if (c + 2 < nchunks) load(va, c + 2);
+    if (c + 3 < nchunks) offsets(c + 3);
+    __syncthreads();
+    store(vb, c + 1);
   }
 }
 
