@@ -96,6 +96,14 @@ SMALL = {
                                                            num_q_heads=8, n_max=64, prefill_max=9000),
     "multipass_trigger": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
                                                              num_q_heads=8, n_max=300),
+    # the multi-pass form with d = 64 and b = 32 (one 64-column half, two 8-row groups per
+    # block), and with the Qwen2 grouping G_q = 7 (w = 16: 112 window rows, 16 padding rows of
+    # the MMA) at a decode trigger of L = 5120
+    "multipass_d64_b32": synth.WORKLOADS["tiny"].scaled(num_requests=3, num_layers=1, num_q_heads=8, num_kv_heads=2,
+                                                        block_size=32, n_max=20, window=4, prefill_max=6000,
+                                                        global_init="uniform"),
+    "multipass_gq7": synth.WORKLOADS["qwen2_7b"].scaled(num_requests=1, num_layers=1, num_q_heads=14,
+                                                        num_kv_heads=2, n_max=160),
 }
 
 
