@@ -406,19 +406,28 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   }
   const int L = m.L, E = L - m.k_r;
   const float* S = sc.score + static_cast<int64_t>(unit) * a.L;
-  const int p0 = tid * kPer;  // this thread's positions [p0, p0 + kPer)
-  // radix select of the E-th smallest key, 8 bits at a time from the top
+  const int p0 = tid * kPer;  // this thread's positions [p0, p0 + kPer) for the destinations
+  // radix select of the E-th smallest key, 8 bits at a time from the top.  The passes read the
+  // scores from registers, loaded once with positions tid + e * kSelThreads (coalesced, every
+  // thread busy).  (Aggregating each warp's adds per distinct bin with a match was slower.)
+  float sv[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int t = tid + e * kSelThreads;
+    sv[e] = t < L ? S[t] : 0.0f;
+  }
   unsigned long long prefix = 0, mask = 0;
   unsigned rank = static_cast<unsigned>(E);
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
+#pragma unroll
     for (int e = 0; e < kPer; ++e) {
-      const int t = p0 + e;
-      if (t >= L) break;
-      const unsigned long long key = evict_key(S[t], t);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFF], 1u);
+      const int t = tid + e * kSelThreads;
+      if (e * kSelThreads >= L) break;  // uniform over the CTA
+      const unsigned long long key = evict_key(sv[e], t);
+      if (t < L && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFF], 1u);
     }
     __syncthreads();
     if (warp == 0) {
