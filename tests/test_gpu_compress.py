@@ -239,7 +239,7 @@ def test_wrong_seq_len_is_reported(zp, bad_len):
 
 # ------------------------------------------------------------------ full-size workloads -----
 
-FULL = ["qwen2_7b", "llama3_8b", "shared_prefix", "prefill"]
+FULL = ["qwen2_7b", "llama3_8b", "shared_prefix", "prefill", "prefill_long"]
 
 
 def _compaction_property_all_units(batch, pristine, keep):
