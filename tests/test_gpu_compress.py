@@ -343,3 +343,37 @@ def test_layer_by_layer_equals_one_call(zp):
         parts.launch(layers=(3, 2))  # past the last layer
     whole.close()
     parts.close()
+
+
+def _random_config(seed):
+    """A seeded random small configuration inside the library's limits: d in {64, 128},
+    b in {16, 32}, G_q in {1, 2, 4, 7, 8}, w with w*G_q <= 128 and w <= k, budgets, prefill
+    lengths (one or several CTAs, or the multi-pass form), shared leading blocks, masks and
+    weights."""
+    rng = np.random.default_rng(seed)
+    d = int(rng.choice([64, 128]))
+    b = int(rng.choice([16, 32]))
+    gq = int(rng.choice([1, 2, 4, 7, 8]))
+    hkv = int(rng.choice([1, 2]))
+    n_max = int(rng.integers(3, 41))
+    k = (n_max - 1) * b
+    w = int(rng.integers(1, min(128 // gq, k) + 1))
+    kind = rng.choice(["trigger", "prefill", "budgets", "prefix"])
+    kw = dict(num_requests=int(rng.integers(1, 4)), num_layers=int(rng.integers(1, 3)), num_q_heads=gq * hkv,
+              num_kv_heads=hkv, head_dim=d, block_size=b, n_max=n_max, window=w,
+              key_recipe=str(rng.choice(["normal", "clustered", "rope"])), global_init="uniform",
+              alpha=float(rng.uniform(0, 1)), beta=float(rng.uniform(0, 1)), decay=float(rng.uniform(0.5, 1)),
+              protect_window=int(rng.integers(0, 2)), causal=int(rng.integers(0, 2)))
+    if kind == "prefill":
+        kw["prefill_max"] = int(rng.choice([k + 2 * b, 2 * n_max * b, 4500, 6000]))
+    elif kind == "budgets" and n_max > 3:
+        kw["budget_min"] = 3
+    elif kind == "prefix" and n_max > 4:
+        kw["shared_prefix_blocks"] = int(rng.integers(1, n_max - 2))
+    return synth.WORKLOADS["tiny"].scaled(**kw)
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_configurations_match_oracle(zp, seed):
+    wl = _random_config(1000 + seed)
+    assert _check_all(zp, wl) <= 2, wl
