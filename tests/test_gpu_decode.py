@@ -61,6 +61,19 @@ def test_decode_matches_oracle(zp, Hq, Hkv, d, b):
     _decode_case(zipage, Hq, Hkv, d, b, [1, b - 1, b, b + 1, 255, 256, 257, 700])
 
 
+@pytest.mark.parametrize("seed", range(16))
+def test_decode_random_configurations(zp, seed):
+    # seeded shapes and lengths: G_q in {1, 2, 4, 7, 8}, d in {64, 128}, b in {16, 32}, batches
+    # of 1..9 requests with lengths from 1 token to several splits (split = 32 blocks)
+    zipage, _ = zp
+    rng = np.random.default_rng(2000 + seed)
+    g = int(rng.choice([1, 2, 4, 7, 8]))
+    hkv = int(rng.choice([1, 2, 4]))
+    d, b = int(rng.choice([64, 128])), int(rng.choice([16, 32]))
+    lens = [int(x) for x in rng.integers(1, int(rng.choice([64, 600, 3000])) + 1, size=int(rng.integers(1, 10)))]
+    _decode_case(zipage, g * hkv, hkv, d, b, lens, layers=int(rng.integers(1, 3)), seed=seed, layer=0)
+
+
 def test_decode_long_sequences_many_splits(zp):
     zipage, _ = zp
     _decode_case(zipage, 32, 8, 128, 16, [2048, 2047, 1500, 33], seed=3)
