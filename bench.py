@@ -271,9 +271,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "compressions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 K/V/Q, fp32 scores", "data": "synthetic (seeded)",
-        "config": {"workload": f"{wl.name}: {inp.num_compress} requests x {wl.num_layers} layers, "
-                               f"Hq {wl.num_q_heads}/Hkv {wl.num_kv_heads}, d {wl.head_dim}, b {wl.block_size}, "
-                               f"N_max {wl.n_max}, w {wl.window}",
+        "config": {"workload": workload_name(wl, inp.num_compress),
                    "compressions_per_step": compressions, "units_per_step": compressions * wl.num_kv_heads,
                    "moved_rows_per_step": moved,
                    "l2": "pool + global scores restored from a pristine device copy before every step "
@@ -543,6 +541,12 @@ def run_mixed(args):
     batch.close()
 
 
+def workload_name(wl, num_compress):
+    """The workload as both arms name it in `config`."""
+    return (f"{wl.name}: {num_compress} requests x {wl.num_layers} layers, Hq {wl.num_q_heads}/Hkv "
+            f"{wl.num_kv_heads}, d {wl.head_dim}, b {wl.block_size}, N_max {wl.n_max}, w {wl.window}")
+
+
 def workload_of(args):
     from paged_kv_cache_obs_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
@@ -575,9 +579,13 @@ def run_reference(args):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "compressions/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-           "config": {"workload": f"{wl.name} (sample of {per_step} compressions per step)"},
+           "config": {"workload": workload_name(wl, wl.num_requests),
+                      "compressions_per_step": wl.num_requests * wl.num_layers,
+                      "units_per_step": wl.num_requests * wl.num_layers * wl.num_kv_heads,
+                      "parallelism": "host cores (the fp64 oracle; rank 0 only)"},
            "cpu_baseline": {"value": value, "unit": "compressions/s", "cores": cores, "kind": "oracle",
-                            "sample": f"{per_step} compressions per step (request x layer, all kv heads)"},
+                            "sample": f"{per_step} compressions per step (request x layer, all kv heads) of "
+                                      f"requests 0 and 1, timed and scaled to compressions/s"},
            "e2e": {"value": value, "unit": "compressions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
