@@ -311,6 +311,15 @@ def test_pass_invariants(prefix):
         assert not set(fresh.ravel().tolist()) & set(np.nonzero(inp.refcount)[0].tolist())
 
 
+def test_slot_location_hand_example():
+    # Paged storage (zh 2.3 "PagedAttention"): logical slot t lives in row t mod b of the block
+    # the table names at position t div b.  b = 4, table [7, 3, 9]:
+    table = np.array([7, 3, 9])
+    assert O.slot_location(table, 0, 4) == (7, 0)
+    assert O.slot_location(table, 5, 4) == (3, 1)    # second block, second row
+    assert O.slot_location(table, 11, 4) == (9, 3)   # third block, last row
+
+
 def test_pass_is_per_head_independent():
     # Changing one head's keys changes only that head's selection.
     wl = _small_llama(num_requests=1, num_layers=1, n_max=4)
