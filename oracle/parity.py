@@ -25,12 +25,13 @@ ATOL = 1e-6
 
 
 def within_tol(x, ref):
+    """Elementwise: |x - ref| <= RTOL*|ref| + ATOL for a finite reference; an infinite
+    reference (a protected window token's score, fr 2.A) must be matched exactly."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
-    both_inf = np.isinf(x) & np.isinf(ref) & (np.sign(x) == np.sign(ref))
     with np.errstate(invalid="ignore"):
-        ok = both_inf | (np.abs(x - ref) <= RTOL * np.abs(ref) + ATOL)
-    return ok
+        close = np.abs(x - ref) <= RTOL * np.abs(ref) + ATOL
+    return np.where(np.isfinite(ref), close, x == ref)
 
 
 def assert_close(name, x, ref, where=""):
