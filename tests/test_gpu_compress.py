@@ -377,3 +377,55 @@ def _random_config(seed):
 def test_random_configurations_match_oracle(zp, seed):
     wl = _random_config(1000 + seed)
     assert _check_all(zp, wl) <= 2, wl
+
+
+BAD_KINDS = ["src_past_pool", "src_negative", "dst_past_pool", "qslot_past_slots", "qslot_negative"]
+
+
+@pytest.mark.parametrize("path", ["fused", "multipass"])
+@pytest.mark.parametrize("kind", BAD_KINDS)
+def test_bad_metadata_skips_only_that_request(zp, kind, path):
+    # request 1 carries one bad entry: the call reports ZP_ERR_BAD_TABLE, request 1's blocks and
+    # global scores stay as they were, and request 0 is compressed exactly as the oracle says
+    zipage, runner = zp
+    if path == "fused":
+        wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, num_kv_heads=2, num_q_heads=8,
+                                                 n_max=16)
+    else:
+        wl = synth.WORKLOADS["prefill"].scaled(num_requests=2, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                               n_max=64, prefill_max=5000)
+    inp = synth.make_inputs(wl, "cpu")
+    pool_in = synth.bf16_bits(inp.pool)
+    gs_in = inp.global_scores.numpy().copy()
+    batch = runner.CompressionBatch(inp, "cuda")
+    batch.enable_debug()
+    NB = inp.pool.shape[1]
+    if kind.startswith("src"):
+        t = batch.d_tables.clone()
+        t[1, 2] = NB + 5 if kind == "src_past_pool" else -3
+        batch.d_tables = t
+    elif kind == "dst_past_pool":
+        t = batch.d_dst.clone()
+        t[1, 1] = NB + 7
+        batch.d_dst = t
+    else:
+        q = batch.d_qslot.clone()
+        q[1] = inp.obs_q.shape[0] + 2 if kind == "qslot_past_slots" else -1
+        batch.d_qslot = q
+    batch.launch()
+    assert batch.error() == zipage.ZP_ERR_BAD_TABLE
+    torch.cuda.synchronize()
+    out = synth.bf16_bits(batch.pool)
+    L1 = int(inp.seq_len[1])
+    blocks1 = set(inp.block_tables[1, :(L1 + wl.block_size - 1) // wl.block_size].tolist())
+    blocks1 |= set(batch.dst_tables[1, :wl.n_max - 1].tolist())
+    for blk in blocks1:
+        assert np.array_equal(out[:, blk], pool_in[:, blk]), blk
+    assert np.array_equal(batch.gs.cpu().numpy()[1], gs_in[1])
+    # request 0 against the oracle, unit by unit
+    dbg = {k: v.cpu().numpy() for k, v in batch.debug.items()}
+    units = [(0, l, h) for l in range(wl.num_layers) for h in range(wl.num_kv_heads)]
+    ndiff = parity.check_units(units, pool_in, synth.bf16_bits(inp.obs_q), gs_in, batch.tables, batch.dst_tables,
+                               inp.seq_len[:2], inp.qslot, wl.params(), dbg, batch.gs.cpu().numpy(), out)
+    assert ndiff <= 2
+    batch.close()
