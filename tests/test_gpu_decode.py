@@ -93,6 +93,34 @@ def test_decode_bad_block_id_reports(zp):
     assert zipage.zp_read_error(ws) == zipage.ZP_ERR_BAD_TABLE
 
 
+@pytest.mark.parametrize("bad_seq", [0, -4, 4 * 16 + 1])
+def test_decode_bad_seq_len_reports_and_keeps_the_others(zp, bad_seq):
+    # request 1's length is outside 1 .. max_blocks*b: the call reports it and leaves its output
+    # untouched; requests 0 and 2 are decoded as the oracle says
+    zipage, _ = zp
+    g = torch.Generator().manual_seed(5)
+    p = dict(num_layers=1, num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16, n_max=4, window=1,
+             alpha=0.5, beta=0.5, decay=0.9, scale=0.125, protect_window=1, causal=1)
+    pool = torch.randn((1, 12, 2, 2, 16, 64), generator=g).to(torch.bfloat16)
+    tables = torch.tensor([[0, 1, 2, 3], [4, 5, 6, 7], [8, 9, 10, 11]], dtype=torch.int32)
+    seq = torch.tensor([37, bad_seq, 64], dtype=torch.int32)
+    q = torch.randn((3, 4, 64), generator=g).to(torch.bfloat16)
+    out = torch.full((3, 4, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, 3, 4))
+    zipage.zp_paged_decode_attn(pool.cuda(), 0, q.cuda(), tables.cuda(), seq.cuda(), out, p, ws)
+    assert zipage.zp_read_error(ws) == zipage.ZP_ERR_BAD_TABLE
+    got = out.float().cpu()
+    assert bool((got[1] == 7.0).all())
+    pb, qb = synth.bf16_bits(pool), synth.bf16_bits(q)
+    for r in (0, 2):
+        for h in range(2):
+            k = O.gather_rows(pb, 0, 0, h, tables[r].numpy(), int(seq[r]), 16)
+            v = O.gather_rows(pb, 0, 1, h, tables[r].numpy(), int(seq[r]), 16)
+            want = O.decode_attention(qb[r, 2 * h:2 * h + 2], k, v, p["scale"])
+            err = np.abs(got[r, 2 * h:2 * h + 2].numpy() - want)
+            assert (err <= DEC_RTOL * np.abs(want) + DEC_ATOL).all(), (r, h)
+
+
 def test_mixed_step_side_stream(zp):
     """Compression of the slot holders on a side stream, decode of the others on the main
     stream, then the event-deferred release of the last blocks."""
