@@ -27,7 +27,10 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kBlocksPerSplit = 32;  // KV blocks per CTA (<= 32 * kWarps)
+// KV blocks per CTA (a split): 32, 64 or 128 (<= 32 * kWarps: a lane holds each block id of
+// its warp), chosen per launch; workspaces are sized for the smallest
+constexpr int kMinBlocksPerSplit = 32;
+constexpr int kMaxBlocksPerSplit = 32 * kWarps;
 constexpr int kChunkRows = 16;       // rows per bulk-copied K (and V) chunk: b = 16 or 32
 constexpr uint64_t kWaitNsD = 2000000000ull;
 
@@ -41,6 +44,7 @@ struct DecodeArgs {
   float* part;  // [B][Hq][max_splits][d + 2]
   int32_t* err;
   int B, layer, Hq, Hkv, d, b, Gq, max_blocks, max_splits;
+  int bps;    // blocks per split of this launch
   float sl2;  // scale * log2(e)
 };
 
@@ -97,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int b = a.b;
   const int cpb = b / kChunkRows;              // chunks per block
   const int nblk = (seq + b - 1) / b;
-  const int blk0 = split * kBlocksPerSplit;
-  const int blk1 = min(nblk, blk0 + kBlocksPerSplit);
+  const int blk0 = split * a.bps;
+  const int blk1 = min(nblk, blk0 + a.bps);
 
   if (tid == 0) sm_bad = (seq < 1 || seq > a.max_blocks * b) ? 1 : 0;
   if (lane == 0) {
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
 
   // This warp's blocks are blk0 + warp + kWarps*i (i < nb); lane i holds the physical id of
-  // the i-th one (kBlocksPerSplit / kWarps <= 32), so issuing a copy needs no global load.
+  // the i-th one (a split's blocks / kWarps <= 32), so issuing a copy needs no global load.
   const int nb = (blk1 - blk0 - warp + kWarps - 1) / kWarps;  // may be <= 0
   const int32_t* table = a.tables + static_cast<int64_t>(r) * a.max_blocks;
   const int my_phys = (lane < nb) ? table[blk0 + warp + kWarps * lane] : 0;
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   __syncthreads();
   // merge the warps: thread -> (g, dim) pairs; a request of one split writes its output here,
   // longer ones write partials for decode_combine_kernel
-  const bool single = nblk <= kBlocksPerSplit;
+  const bool single = nblk <= a.bps;
   for (int idx = tid; idx < G * D; idx += kThreads) {
     const int g = idx / D, dim = idx % D;
     float M = -INFINITY;
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
   const int seq = a.seq_lens[r];
   if (seq < 1 || seq > a.max_blocks * a.b) return;
   const int nblk = (seq + a.b - 1) / a.b;
-  const int ns = (nblk + kBlocksPerSplit - 1) / kBlocksPerSplit;
+  const int ns = (nblk + a.bps - 1) / a.bps;
   if (ns == 1) return;  // written by the decode kernel itself
   const float* p = a.part + (static_cast<int64_t>(r) * a.Hq + qh) * a.max_splits * (D + 2);
   float M = -INFINITY;
@@ -340,7 +344,7 @@ cudaError_t dispatch_g(const CUtensorMap& tm, const DecodeArgs& a, cudaStream_t 
 
 }  // namespace
 
-int decode_max_splits(int max_blocks) { return (max_blocks + kBlocksPerSplit - 1) / kBlocksPerSplit; }
+int decode_max_splits(int max_blocks) { return (max_blocks + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit; }
 
 zp_status decode_validate(const zp_kv_pool* pool, int32_t layer, const uint16_t* q, const int32_t* block_tables,
                           const int32_t* seq_lens, int32_t B, int32_t max_blocks, const uint16_t* out,
@@ -379,7 +383,15 @@ zp_status decode_launch(const zp_kv_pool* pool, int32_t layer, const uint16_t* q
   a.b = p->block_size;
   a.Gq = p->num_q_heads / p->num_kv_heads;
   a.max_blocks = max_blocks;
-  a.max_splits = decode_max_splits(max_blocks);
+  // the longest split that still gives about two waves of CTAs (three CTAs per SM): fewer
+  // splits mean fewer partials to merge, more splits keep every SM busy on small batches
+  a.bps = kMinBlocksPerSplit;
+  for (int bps = kMaxBlocksPerSplit; bps > kMinBlocksPerSplit; bps >>= 1)
+    if (static_cast<int64_t>(B) * a.Hkv * ((max_blocks + bps - 1) / bps) >= 6LL * num_sms()) {
+      a.bps = bps;
+      break;
+    }
+  a.max_splits = (max_blocks + a.bps - 1) / a.bps;
   a.sl2 = p->scale * 1.4426950408889634f;
   if (B == 0) return ZP_OK;
   // the pool as {d, 2*Hkv*b rows per (layer, block), layers*num_blocks}; box = 16 rows of one
