@@ -536,7 +536,7 @@ def run_mixed(args):
            "mixed": {"compress_ms": tc, "decode_ms": td, "both_ms": tb,
                      "overlap_frac": (tc + td - tb) / min(tc, td),
                      "decode_hbm_gbs": dec_bytes / (td / 1e3) / 1e9, "decode_tokens_per_layer": dec_tokens},
-           "gpu_launches": 1 + 2 * wl.num_layers}
+           "gpu_launches": 1 + wl.num_layers * zipage.zp_paged_decode_kernel_launches(p, nd, dec_tables.shape[1])}
     print(json.dumps(out), flush=True)
     batch.close()
 

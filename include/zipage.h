@@ -196,6 +196,12 @@ zp_status zp_paged_decode_attn(const zp_kv_pool* pool, int32_t layer, const uint
 
 size_t zp_paged_decode_workspace_size(const zp_params* params, int32_t B, int32_t max_blocks);
 
+/* Kernel launches one zp_paged_decode_attn call with these sizes makes on the current device:
+ * 1 when every request fits one split (the split size is chosen per call from B, H_kv,
+ * max_blocks and the device's SM count), 2 with the kernel that merges the splits.  0 for
+ * invalid arguments.  Host only; launches nothing. */
+int32_t zp_paged_decode_kernel_launches(const zp_params* params, int32_t B, int32_t max_blocks);
+
 /* ---------------------------------------------------------------------------------------
  * zp_paged_decode_attn without any device allocation by anyone.  The paper has no
  * counterpart: this is a convenience of this library.

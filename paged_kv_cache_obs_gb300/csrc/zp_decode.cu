@@ -346,6 +346,15 @@ cudaError_t dispatch_g(const CUtensorMap& tm, const DecodeArgs& a, cudaStream_t 
 
 int decode_max_splits(int max_blocks) { return (max_blocks + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit; }
 
+// Blocks per split of a launch: the longest split that still gives about two waves of CTAs
+// (three CTAs per SM).  Fewer splits mean fewer partials to merge; more splits keep every SM
+// busy on small batches.
+int decode_blocks_per_split(int B, int Hkv, int max_blocks) {
+  for (int bps = kMaxBlocksPerSplit; bps > kMinBlocksPerSplit; bps >>= 1)
+    if (static_cast<int64_t>(B) * Hkv * ((max_blocks + bps - 1) / bps) >= 6LL * num_sms()) return bps;
+  return kMinBlocksPerSplit;
+}
+
 zp_status decode_validate(const zp_kv_pool* pool, int32_t layer, const uint16_t* q, const int32_t* block_tables,
                           const int32_t* seq_lens, int32_t B, int32_t max_blocks, const uint16_t* out,
                           const zp_params* p) {
@@ -383,14 +392,7 @@ zp_status decode_launch(const zp_kv_pool* pool, int32_t layer, const uint16_t* q
   a.b = p->block_size;
   a.Gq = p->num_q_heads / p->num_kv_heads;
   a.max_blocks = max_blocks;
-  // the longest split that still gives about two waves of CTAs (three CTAs per SM): fewer
-  // splits mean fewer partials to merge, more splits keep every SM busy on small batches
-  a.bps = kMinBlocksPerSplit;
-  for (int bps = kMaxBlocksPerSplit; bps > kMinBlocksPerSplit; bps >>= 1)
-    if (static_cast<int64_t>(B) * a.Hkv * ((max_blocks + bps - 1) / bps) >= 6LL * num_sms()) {
-      a.bps = bps;
-      break;
-    }
+  a.bps = decode_blocks_per_split(B, a.Hkv, max_blocks);
   a.max_splits = (max_blocks + a.bps - 1) / a.bps;
   a.sl2 = p->scale * 1.4426950408889634f;
   if (B == 0) return ZP_OK;
@@ -408,6 +410,12 @@ zp_status decode_launch(const zp_kv_pool* pool, int32_t layer, const uint16_t* q
 }  // namespace zp
 
 using namespace zp;
+
+extern "C" int32_t zp_paged_decode_kernel_launches(const zp_params* p, int32_t B, int32_t max_blocks) {
+  if (!p || B < 1 || max_blocks < 1 || p->num_kv_heads < 1) return 0;
+  const int bps = decode_blocks_per_split(B, p->num_kv_heads, max_blocks);
+  return (max_blocks + bps - 1) / bps > 1 ? 2 : 1;
+}
 
 extern "C" size_t zp_paged_decode_workspace_size(const zp_params* p, int32_t B, int32_t max_blocks) {
   if (!p || B < 0 || max_blocks < 1) return 0;

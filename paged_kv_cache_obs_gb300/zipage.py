@@ -84,6 +84,7 @@ _sig("zp_compress_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_paged_decode_attn", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                     ctypes.POINTER(zp_params), _P, _SZ, _P])
 _sig("zp_paged_decode_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
+_sig("zp_paged_decode_kernel_launches", _I32, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_paged_decode_attn_static", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                            ctypes.POINTER(zp_params), _P, _P])
 _sig("zp_redundancy_all_pairs", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta),
@@ -221,6 +222,10 @@ def zp_redundancy_all_pairs(pool, block_tables, seq_len, redund, params: dict, w
 
 def zp_paged_decode_workspace_size(params: dict, B: int, max_blocks: int) -> int:
     return lib.zp_paged_decode_workspace_size(ctypes.byref(make_params(params)), B, max_blocks)
+
+
+def zp_paged_decode_kernel_launches(params: dict, B: int, max_blocks: int) -> int:
+    return lib.zp_paged_decode_kernel_launches(ctypes.byref(make_params(params)), B, max_blocks)
 
 
 def zp_paged_decode_attn(pool, layer: int, q, block_tables, seq_lens, out, params: dict, workspace,
