@@ -157,6 +157,13 @@ def test_invalid_arguments_are_rejected_without_a_gpu(zp):
     assert st == zp.ZP_ERR_INVALID_ARG
     assert zp.zp_compress_workspace_size(p, 4) >= 4
     assert zp.zp_paged_decode_workspace_size(dict(p, num_kv_heads=2), 3, 20) > 256
+    # decode launch count: 1 or 2 for valid sizes, 0 otherwise; a request of at most 32 blocks
+    # is always one split
+    q = dict(p, num_kv_heads=2)
+    assert zp.zp_paged_decode_kernel_launches(q, 3, 20) == 1
+    assert zp.zp_paged_decode_kernel_launches(q, 3, 4096) in (1, 2)
+    assert zp.zp_paged_decode_kernel_launches(q, 0, 20) == 0
+    assert zp.zp_paged_decode_kernel_launches(q, 3, 0) == 0
 
 
 def test_commit_after_prefill_releases_every_block_past_n_max_minus_1(zp):
