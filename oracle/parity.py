@@ -9,7 +9,8 @@ touches the CUDA path.  The acceptance rule:
 * selection: the kernel's kept set must be exactly what the oracle's selection rule gives on
   the kernel's own fp32 scores (the decision taken in the kernel's precision), and may differ
   from the oracle's fp64 selection only for tokens whose oracle score lies within twice that
-  tolerance of the oracle's keep/evict boundary;
+  tolerance of the oracle's keep/evict boundary (a kept/evicted pair can swap only if the two
+  oracle scores differ by at most the sum of their two tolerances);
 * compaction: given the kernel's kept set, every compacted K/V row is bit-identical to the
   input row it came from, and every byte of the pool that is not a destination row is
   unchanged.

@@ -15,7 +15,8 @@ from oracle import zipage_oracle as O
 
 PINS = (
     [(P.test_two_block_hand_example_attention, {}), (P.test_two_block_hand_example_redundancy, {})]
-    + [(P.test_two_block_hand_example_scores_and_selection, {"case": c}) for c in range(4)]
+    + [(P.test_two_block_hand_example_scores_and_selection, {"case": c}) for c in range(5)]
+    + [(P.test_two_block_hand_example_global_update, {"case": c}) for c in range(5)]
     + [(P.test_attention_mass_is_one, {"causal": c}) for c in (True, False)]
     + [(P.test_identical_keys_causal_closed_form, {}), (P.test_window_row_position_and_mask, {}),
        (P.test_gqa_grouping_is_contiguous, {}), (P.test_redundancy_special_cases, {})]
@@ -102,6 +103,31 @@ def _tail_not_cleared(orig):
     return f
 
 
+def _update_indexed_by_position(orig):
+    # survivor scores left at their source positions t instead of compacted to slots j
+    def f(G, attn, src, decay, L):
+        out = np.zeros(L)
+        src = np.asarray(src)
+        out[src] = decay * np.asarray(G, np.float64)[src] + np.asarray(attn, np.float64)[src]
+        return out
+    return f
+
+
+def _update_attention_of_slot(orig):
+    # slot j takes the attention of position j instead of its source token's
+    def f(G, attn, src, decay, L):
+        out = orig(G, attn, src, decay, L)
+        k = len(src)
+        out[:k] += np.asarray(attn, np.float64)[:k] - np.asarray(attn, np.float64)[np.asarray(src)]
+        return out
+    return f
+
+
+def _update_decay_complement(orig):
+    # (1 - decay) in place of decay
+    return lambda G, attn, src, decay, L: orig(G, attn, src, 1.0 - decay, L)
+
+
 def _shared_blocks_in_place(orig):
     def f(table, n_max, refcount, free_ids):
         return np.array(table[:n_max - 1], dtype=np.int32).copy(), []
@@ -135,6 +161,9 @@ MUTANTS = {
     "lowest scores kept": ("select_keep", _keeps_lowest),
     "decay applied to the attention too": ("global_update", _decay_on_attention),
     "global-score tail not cleared": ("global_update", _tail_not_cleared),
+    "global score left at the source position": ("global_update", _update_indexed_by_position),
+    "global score takes the attention of the slot": ("global_update", _update_attention_of_slot),
+    "global score decayed by 1 - decay": ("global_update", _update_decay_complement),
     "shared prefix blocks compacted in place": ("plan_dst_table", _shared_blocks_in_place),
     "block and row of a slot transposed": ("slot_location", _slot_transposed),
     "query heads grouped interleaved": ("compress_pass", _interleaved_groups),
@@ -150,3 +179,22 @@ def test_planted_mistake_fails_a_pin(monkeypatch, name):
     attr, make = MUTANTS[name]
     monkeypatch.setattr(O, attr, make(getattr(O, attr)))
     assert _failing_pins(), f"no pin catches the planted mistake: {name}"
+
+
+GLOBAL_UPDATE_MUTANTS = ["decay applied to the attention too", "global score left at the source position",
+                         "global score takes the attention of the slot", "global score decayed by 1 - decay"]
+
+
+@pytest.mark.parametrize("name", GLOBAL_UPDATE_MUTANTS)
+def test_global_update_mistake_fails_the_hand_worked_values(monkeypatch, name):
+    # The update rule is pinned by the hand-worked values of the golden file; the pass-level
+    # invariants check only that the pass applies the (pinned) rule to its kept set.
+    attr, make = MUTANTS[name]
+    monkeypatch.setattr(O, attr, make(getattr(O, attr)))
+    failed = []
+    for c in range(5):
+        try:
+            P.test_two_block_hand_example_global_update(case=c)
+        except AssertionError:
+            failed.append(c)
+    assert failed, f"the hand-worked global-score values miss the planted mistake: {name}"

@@ -39,7 +39,7 @@ def test_two_block_hand_example_redundancy():
     np.testing.assert_allclose(O.lightning_redundancy(k, 2), ex["redundancy"], atol=1e-15)
 
 
-@pytest.mark.parametrize("case", range(4))
+@pytest.mark.parametrize("case", range(5))
 def test_two_block_hand_example_scores_and_selection(case):
     ex, q, k = _two_block()
     c = ex["cases"][case]
@@ -50,6 +50,18 @@ def test_two_block_hand_example_scores_and_selection(case):
     want = [math.inf if s == "inf" else s for s in c["S"]]
     np.testing.assert_allclose(S, want, atol=1e-15)
     assert list(O.select_keep(S, ex["k"])) == c["keep"]
+
+
+@pytest.mark.parametrize("case", range(5))
+def test_two_block_hand_example_global_update(case):
+    # The carried global score after the pass (zh 2.1 "global score from historical attention",
+    # fr 2.E), worked by hand in the golden file from the hand-derived attention and keep set:
+    # survivor j carries decay*G + attn of its source token, the freed slots hold 0.
+    ex, _, _ = _two_block()
+    c = ex["cases"][case]
+    got = O.global_update(np.array(c["G"], float), np.array(ex["attn"], float), np.array(c["keep"]),
+                          ex["decay"], ex["L"])
+    np.testing.assert_allclose(got, c["G_new"], rtol=0, atol=1e-15)
 
 
 def _rand_qk(rng, w, G, L, d):
@@ -296,7 +308,10 @@ def test_pass_invariants(prefix):
         v_out = O.gather_rows(new_pool, l, 1, h, dst[r], k, b)
         assert np.array_equal(k_out, k_in[src]) and np.array_equal(v_out, v_in[src])
         G = gs[r, l, h].astype(np.float64)
-        np.testing.assert_allclose(new_G[r, l, h, :k], (0.9 * G[src] + u["attn"][src]).astype(np.float32))
+        # wiring of the pass: the carried score follows the pinned update rule (hand-worked in
+        # test_two_block_hand_example_global_update) on this unit's own kept set and attention
+        want_G = O.global_update(G, u["attn"], src, wl.decay, L)
+        np.testing.assert_allclose(new_G[r, l, h, :k], want_G[:k].astype(np.float32))
         assert (new_G[r, l, h, k:] == 0).all()
     # shared prefix blocks are byte-identical and replaced by fresh targets
     shared = np.nonzero(inp.refcount > 1)[0]
