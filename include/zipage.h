@@ -221,7 +221,10 @@ int32_t zp_paged_decode_kernel_launches(const zp_params* params, int32_t B, int3
  *               cleared on the stream before the kernel runs.  May be NULL, in which case
  *               device-side errors are not reported.
  * The first call on a device looks up the array's device address for that device (with the
- * device current); make that first call before any stream capture.  Every call shares the
+ * device current); make that first call before any stream capture.  The address is kept for
+ * the life of the process: after cudaDeviceReset, or anything else that destroys the device's
+ * primary context, do not call this entry point on that device again in the same process (the
+ * library would be reloaded at an address it does not know).  Every call shares the
  * one array: calls whose kernels may overlap on the GPU (different streams without an
  * ordering between them) race on it and must be serialised by the caller.  The call
  * allocates and frees nothing.
@@ -230,6 +233,21 @@ zp_status zp_paged_decode_attn_static(const zp_kv_pool* pool, int32_t layer, con
                                       const int32_t* block_tables, const int32_t* seq_lens, int32_t B,
                                       int32_t max_blocks, uint16_t* out, const zp_params* params,
                                       int32_t* dev_status, zp_stream stream);
+
+/* Test hook of the device-side failure detection (bounded waits).  Not for production use.
+ * Same operation, arguments and workspace as zp_paged_decode_attn, plus stall_limit_ns
+ * (1 .. 10^9).  Before its first chunk of K/V, every warp of the decode kernel first waits, for
+ * at most stall_limit_ns, on a shared-memory barrier that nothing ever completes.  That wait
+ * runs out, and the kernel then takes the path of any wait that gives up: it waits (bounded,
+ * 2 s) for the copies it has already issued, writes its outputs from the keys it has folded in
+ * (none: zeros) and records ZP_ERR_TIMEOUT in the workspace's error word, which
+ * zp_read_error() returns.  Nothing faults or hangs, and the context stays usable.  Returns
+ * ZP_OK once queued. */
+zp_status zp_test_decode_stalled(const zp_kv_pool* pool, int32_t layer, const uint16_t* q,
+                                 const int32_t* block_tables, const int32_t* seq_lens, int32_t B,
+                                 int32_t max_blocks, uint16_t* out, const zp_params* params,
+                                 void* workspace, size_t workspace_bytes, int64_t stall_limit_ns,
+                                 zp_stream stream);
 
 /* Synchronises `stream`, copies the error word at the start of `workspace` to *out_status and
  * clears it.  Returns ZP_ERR_CUDA if the copy fails. */

@@ -697,13 +697,13 @@ template <int MAXC>
 zp_status launch_compress(const CUtensorMap& tmK, const CUtensorMap& tmQ, const CompressArgs& a, int C,
                           int64_t num_units, cudaStream_t st) {
   const size_t smem = compress_smem_bytes<MAXC>();
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(compress_kernel<MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem));
-    if (attr_err == cudaSuccess && MAXC > 8)
-      attr_err = cudaFuncSetAttribute(compress_kernel<MAXC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  static PerDeviceInit attrs;
+  const cudaError_t attr_err = attrs.run([&] {
+    cudaError_t e = cudaFuncSetAttribute(compress_kernel<MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e == cudaSuccess && MAXC > 8)
+      e = cudaFuncSetAttribute(compress_kernel<MAXC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
   });
   if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
   cudaLaunchConfig_t cfg{};

@@ -622,12 +622,13 @@ zp_status launch_compress_long(const CUtensorMap& tmK, const CUtensorMap& tmQ, c
   sc.src = reinterpret_cast<int32_t*>(p);
   if (units * sc.nch >= (int64_t(1) << 31)) return ZP_ERR_UNSUPPORTED;
   const size_t smem = sizeof(LongSmem) + 1024;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(long_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(long_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static PerDeviceInit attrs;
+  const cudaError_t attr = attrs.run([&] {
+    cudaError_t e =
+        cudaFuncSetAttribute(long_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(long_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    return e;
   });
   if (attr != cudaSuccess) return ZP_ERR_CUDA;
   const unsigned chunks = static_cast<unsigned>(units * sc.ngrp);

@@ -46,6 +46,9 @@ struct DecodeArgs {
   int B, layer, Hq, Hkv, d, b, Gq, max_blocks, max_splits;
   int bps;    // blocks per split of this launch
   float sl2;  // scale * log2(e)
+  // test hook of the bounded waits, 0 in normal calls: before its first chunk every warp also
+  // waits this long on a barrier that nothing completes, so the wait runs out
+  uint64_t stall_ns;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -88,6 +91,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   __shared__ float sm_acc[kWarps][G][D];
   __shared__ int sm_bad;
   __shared__ __align__(8) uint64_t sm_bar[kWarps][2];
+  __shared__ __align__(8) uint64_t sm_never;  // test hook: no thread or copy ever arrives on it
   // per warp, two stages of (K, V) chunks of kChunkRows rows in the TMA's 128-byte swizzle
   // (dynamic shared memory, 1024-byte aligned below)
   extern __shared__ uint8_t dyn_smem[];
@@ -104,7 +108,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int blk0 = split * a.bps;
   const int blk1 = min(nblk, blk0 + a.bps);
 
-  if (tid == 0) sm_bad = (seq < 1 || seq > a.max_blocks * b) ? 1 : 0;
+  if (tid == 0) {
+    sm_bad = (seq < 1 || seq > a.max_blocks * b) ? 1 : 0;
+    mbar_init(&sm_never, 1);
+  }
   if (lane == 0) {
     mbar_init(&sm_bar[warp][0], 1);
     mbar_init(&sm_bar[warp][1], 1);
@@ -175,7 +182,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   for (; c < nch; ++c) {
     const int st = c & 1;
     bool w = true;
-    if (lane == 0) w = mbar_wait_bounded(&sm_bar[warp][st], (ph >> st) & 1u, kWaitNsD);
+    if (lane == 0) {
+      if (a.stall_ns != 0 && c == 0) w = mbar_wait_bounded(&sm_never, 0u, a.stall_ns);  // runs out
+      if (w) w = mbar_wait_bounded(&sm_bar[warp][st], (ph >> st) & 1u, kWaitNsD);
+    }
     w = __shfl_sync(0xffffffffu, w, 0);
     if (!w) {
       ok = false;
@@ -319,11 +329,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a) {
 template <int D, int G>
 cudaError_t launch_decode(const CUtensorMap& tm, const DecodeArgs& a, cudaStream_t st) {
   constexpr int kv_bytes = kWarps * 2 * 2 * kChunkRows * D * 2 + 1024;  // + alignment slack
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
-  });
+  static PerDeviceInit attrs;
+  const cudaError_t attr = attrs.run(
+      [] { return cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes); });
   if (attr != cudaSuccess) return attr;
   decode_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kThreads, kv_bytes, st>>>(tm, a);
   if (a.max_splits > 1) decode_combine_kernel<D><<<dim3(a.Hq, a.B), D, 0, st>>>(a);
@@ -374,7 +382,7 @@ zp_status decode_validate(const zp_kv_pool* pool, int32_t layer, const uint16_t*
 // Launches the decode kernels with partials in `part` and the error word at `err`.
 zp_status decode_launch(const zp_kv_pool* pool, int32_t layer, const uint16_t* q, const int32_t* block_tables,
                         const int32_t* seq_lens, int32_t B, int32_t max_blocks, uint16_t* out, const zp_params* p,
-                        float* part, int32_t* err, cudaStream_t st) {
+                        float* part, int32_t* err, cudaStream_t st, uint64_t stall_ns = 0) {
   DecodeArgs a{};
   a.pool = static_cast<const uint8_t*>(pool->base);
   a.num_blocks = pool->num_blocks;
@@ -395,6 +403,7 @@ zp_status decode_launch(const zp_kv_pool* pool, int32_t layer, const uint16_t* q
   a.bps = decode_blocks_per_split(B, a.Hkv, max_blocks);
   a.max_splits = (max_blocks + a.bps - 1) / a.bps;
   a.sl2 = p->scale * 1.4426950408889634f;
+  a.stall_ns = stall_ns;
   if (B == 0) return ZP_OK;
   // the pool as {d, 2*Hkv*b rows per (layer, block), layers*num_blocks}; box = 16 rows of one
   // (K or V, head) tile, 64 columns, 128-byte swizzle
@@ -437,6 +446,24 @@ extern "C" zp_status zp_paged_decode_attn(const zp_kv_pool* pool, int32_t layer,
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
   return decode_launch(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p, part,
                        static_cast<int32_t*>(workspace), st);
+}
+
+extern "C" zp_status zp_test_decode_stalled(const zp_kv_pool* pool, int32_t layer, const uint16_t* q,
+                                            const int32_t* block_tables, const int32_t* seq_lens, int32_t B,
+                                            int32_t max_blocks, uint16_t* out, const zp_params* p,
+                                            void* workspace, size_t workspace_bytes, int64_t stall_limit_ns,
+                                            zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_test_decode_stalled");
+  if (stall_limit_ns < 1 || stall_limit_ns > 1000000000LL) return ZP_ERR_INVALID_ARG;
+  zp_status s = decode_validate(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p);
+  if (s != ZP_OK) return s;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < zp_paged_decode_workspace_size(p, B, max_blocks))
+    return ZP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 4, st) != cudaSuccess) return ZP_ERR_CUDA;
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+  return decode_launch(pool, layer, q, block_tables, seq_lens, B, max_blocks, out, p, part,
+                       static_cast<int32_t*>(workspace), st, static_cast<uint64_t>(stall_limit_ns));
 }
 
 // ------------------------------------------------------------------ no-allocation variant ----

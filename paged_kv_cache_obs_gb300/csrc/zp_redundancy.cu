@@ -375,11 +375,10 @@ extern "C" zp_status zp_redundancy_all_pairs(const zp_kv_pool* pool, const int32
   a.nt = nt;
 
   const size_t smem = sizeof(ApSmem) + 1024;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(all_pairs_redundancy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem));
+  static PerDeviceInit attrs;
+  const cudaError_t attr_err = attrs.run([&] {
+    return cudaFuncSetAttribute(all_pairs_redundancy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
   });
   if (attr_err != cudaSuccess) return ZP_ERR_CUDA;
   key_sq_norm_kernel<<<static_cast<unsigned>(ctas), kThreadsA, 0, st>>>(a);

@@ -87,6 +87,8 @@ _sig("zp_paged_decode_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I
 _sig("zp_paged_decode_kernel_launches", _I32, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_paged_decode_attn_static", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                            ctypes.POINTER(zp_params), _P, _P])
+_sig("zp_test_decode_stalled", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
+                                      ctypes.POINTER(zp_params), _P, _SZ, _I64, _P])
 _sig("zp_redundancy_all_pairs", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta),
                                        ctypes.POINTER(zp_params), _P, _P, _SZ, _P])
 _sig("zp_redundancy_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
@@ -236,6 +238,19 @@ def zp_paged_decode_attn(pool, layer: int, q, block_tables, seq_lens, out, param
                                   ctypes.byref(make_params(params)), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream))
     _check("zp_paged_decode_attn", st)
+
+
+def zp_test_decode_stalled(pool, layer: int, q, block_tables, seq_lens, out, params: dict, workspace,
+                           stall_limit_ns: int, stream=None):
+    """Test hook of the bounded waits: decode attention whose kernel first waits, at most
+    stall_limit_ns, on a barrier nothing completes, and so reports ZP_ERR_TIMEOUT."""
+    kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    st = lib.zp_test_decode_stalled(ctypes.byref(kv), layer, _ptr(q), _ptr(block_tables), _ptr(seq_lens),
+                                    q.shape[0], block_tables.shape[1], _ptr(out),
+                                    ctypes.byref(make_params(params)), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), int(stall_limit_ns),
+                                    _stream(stream))
+    _check("zp_test_decode_stalled", st)
 
 
 def zp_paged_decode_attn_static(pool, layer: int, q, block_tables, seq_lens, out, params: dict,

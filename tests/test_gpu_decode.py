@@ -178,3 +178,61 @@ def test_mixed_step_side_stream(zp):
     parity.check_units(units, pool_in, obs_q, gs_in, batch.tables, batch.dst_tables, inp.seq_len[:R],
                        inp.qslot, p, dbg, batch.gs.cpu().numpy(), synth.bf16_bits(batch.pool), full_pool=True)
     batch.close()
+
+
+def test_mixed_step_full_size(zp):
+    """The mixed serving step at its stated size, run as the benchmark runs it: the 32 slot
+    holders (128 full blocks each) compress on a side stream while decode attention of the 224
+    other requests (U{1..128} blocks) runs for all 32 layers on a high-priority stream, with the
+    split size each decode call chooses.  The pool holds the blocks in use.  Checked: the
+    compaction of every compressed unit (kept count, window, bit-exact rows, untouched blocks),
+    sampled compression units against the oracle, and sampled decode outputs against the oracle
+    (first and last layer, the shortest and longest requests, seeded random others)."""
+    from test_gpu_compress import _compaction_property_all_units, check_sampled_units
+    zipage, runner = zp
+    wl = synth.WORKLOADS["mixed"]
+    inp = synth.make_inputs(wl, "cuda")
+    R, nd, nl = inp.num_compress, wl.num_decode, wl.num_layers
+    assert (R, nd, nl) == (32, 224, 32)
+    pristine = inp.pool.clone()
+    gs_in = inp.global_scores.clone()
+    batch = runner.CompressionBatch(inp, "cuda", pool=inp.pool)
+    batch.enable_debug()
+    p = wl.params()
+    dec_tables = torch.from_numpy(np.ascontiguousarray(inp.block_tables[R:])).cuda()
+    dec_seq = torch.from_numpy(np.ascontiguousarray(inp.seq_len[R:])).cuda()
+    outs = torch.zeros((nl, nd, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, nd, dec_tables.shape[1]))
+    side, main = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1)
+    side.wait_stream(torch.cuda.current_stream())
+    main.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        batch.launch(stream=side)
+    for l in range(nl):
+        zipage.zp_paged_decode_attn(batch.pool, l, inp.decode_q[l], dec_tables, dec_seq, outs[l], p, ws, stream=main)
+    torch.cuda.synchronize()
+    assert batch.error(side) == 0
+    assert zipage.zp_read_error(ws, main) == 0
+    # compression: every unit's compaction, then sampled units against the oracle
+    _compaction_property_all_units(batch, pristine, batch.debug["keep"])
+    check_sampled_units(batch, inp, pristine, gs_in, seed=5)
+    # decode: the decode requests' blocks are disjoint from the compressing ones
+    got = outs.float().cpu().numpy()
+    qb = synth.bf16_bits(inp.decode_q.cpu())
+    G = wl.num_q_heads // wl.num_kv_heads
+    b = wl.block_size
+    dseq = inp.seq_len[R:]
+    rng = np.random.default_rng(9)
+    picks = {(0, int(np.argmin(dseq))), (nl - 1, int(np.argmax(dseq)))}
+    picks |= {(int(rng.integers(nl)), int(rng.integers(nd))) for _ in range(10)}
+    for l, i in sorted(picks):
+        s = int(dseq[i])
+        tab = torch.from_numpy(inp.block_tables[R + i]).long().cuda()
+        t = torch.arange(s, device="cuda")
+        for h in range(wl.num_kv_heads):
+            k = synth.bf16_bits(pristine[l, tab[t // b], 0, h, t % b])
+            v = synth.bf16_bits(pristine[l, tab[t // b], 1, h, t % b])
+            want = O.decode_attention(qb[l, i, h * G:(h + 1) * G], k, v, wl.scale)
+            err = np.abs(got[l, i, h * G:(h + 1) * G] - want)
+            assert (err <= DEC_RTOL * np.abs(want) + DEC_ATOL).all(), (l, i, h, float(err.max()))
+    batch.close()

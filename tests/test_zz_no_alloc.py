@@ -14,9 +14,6 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-# the tolerance of the decode tests: bf16 output rounding (2^-9 relative) plus fp32 accumulation
-RTOL, ATOL = 4e-3, 1e-4
-
 
 @pytest.fixture(scope="module")
 def zipage():
@@ -41,17 +38,19 @@ def _case(seed, seq_lens, Hq=32, Hkv=8, d=128, b=16, layers=2):
     return pool, tables, q, seq, p
 
 
-def _with_workspace(zipage, pool, tables, q, seq, p, layer):
+def _with_workspace(zipage, pool, tables, q, seq, p, layer, expect=0):
     out = torch.zeros_like(q)
     ws = zipage.new_workspace(zipage.zp_paged_decode_workspace_size(p, q.shape[0], tables.shape[1]))
     zipage.zp_paged_decode_attn(pool, layer, q, tables, seq, out, p, ws)
-    assert zipage.zp_read_error(ws) == 0
-    return out.float()
+    assert zipage.zp_read_error(ws) == expect
+    return out
 
 
 def test_static_scratch_matches_workspace_variant_twice(zipage):
-    # call 1 spans several splits per request; call 2 is smaller, so partials left in the
-    # shared array by call 1 would show up if they leaked into call 2
+    # Both entry points run the same kernels with the same split size and differ only in where
+    # the split partials live, so the outputs must be bit-identical.  Call 1 spans several
+    # splits per request; call 2 is smaller, so partials left in the shared array by call 1
+    # would show up if they leaked into call 2.
     cases = [_case(11, [1, 17, 300, 1100, 2048, 513], layers=2), _case(12, [40, 16, 257], layers=3)]
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for (pool, tables, q, seq, p), layer in zip(cases, (1, 2)):
@@ -60,8 +59,32 @@ def test_static_scratch_matches_workspace_variant_twice(zipage):
         zipage.zp_paged_decode_attn_static(pool, layer, q, tables, seq, out, p, dev_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        got = out.float()
-        assert torch.all((got - want).abs() <= RTOL * want.abs() + ATOL)
+        assert torch.equal(out, want)
+
+
+def test_static_scratch_reports_a_bad_request_then_recovers(zipage):
+    # A request whose length exceeds its table is reported through dev_status and left alone;
+    # the other requests are still computed.  The next call, with no status word (device-side
+    # errors go to the array's spare word), starts from a clean state and matches again.
+    pool, tables, q, seq, p = _case(14, [300, 1100, 700, 64], layers=2)
+    max_blocks = tables.shape[1]
+    bad = seq.clone()
+    bad[1] = max_blocks * p["block_size"] + 1
+    want = _with_workspace(zipage, pool, tables, q, bad, p, 1, expect=zipage.ZP_ERR_BAD_TABLE)
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    sentinel = torch.full_like(q, 7.0)
+    out = sentinel.clone()
+    zipage.zp_paged_decode_attn_static(pool, 1, q, tables, bad, out, p, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == zipage.ZP_ERR_BAD_TABLE
+    good = [0, 2, 3]
+    assert torch.equal(out[good], want[good])
+    assert torch.equal(out[1], sentinel[1])          # the bad request's output is untouched
+    want2 = _with_workspace(zipage, pool, tables, q, seq, p, 0)
+    out2 = torch.zeros_like(q)
+    zipage.zp_paged_decode_attn_static(pool, 0, q, tables, seq, out2, p, dev_status=None)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, want2)
 
 
 def test_static_scratch_rejects_calls_beyond_its_size(zipage):
