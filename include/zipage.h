@@ -137,6 +137,10 @@ typedef struct zp_debug {
  *   stream        stream to launch on.
  * Source and destination blocks of different requests must not overlap (shared prefix
  * blocks are only read).  Returns ZP_OK once queued.
+ * A unit with bad metadata (ZP_ERR_BAD_TABLE) is skipped whole and every other unit is
+ * compressed.  ZP_ERR_TIMEOUT (a wait inside the kernel gave up after 2 s, which only a broken
+ * device or driver state produces) means the call failed: the pool and the global scores of
+ * the units the stalled cluster went on to process are undefined.
  * --------------------------------------------------------------------------------------- */
 zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
                       const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
