@@ -23,8 +23,9 @@
 //   4. MMA D2 = K Q^T (M=128 keys, N=128 rows): each thread owns one key and sums its
 //      normalised probabilities over the window rows without shuffles (pass 2).
 //   5. Selection of the E = L-k lowest (S asc, t desc) keys: per-warp bitonic sorts and merge
-//      trees (E <= 32), or a CTA-wide bitonic sort and ranks by binary search in local copies
-//      of every CTA's sorted list (E > 32); every CTA derives the same eviction set.
+//      trees (E <= 32), or per-warp sorts merged by rank into a sorted list per CTA and ranks
+//      by binary search in local copies of every CTA's sorted list (E > 32); every CTA
+//      derives the same eviction set.
 //   6. V rows are staged (shared memory and registers) before a cluster barrier that separates
 //      every read of the unit from every write (compaction is in place, dst <= src); K rows are
 //      written from shared memory, V rows from the staging, G' from registers.
@@ -44,15 +45,18 @@ template <int MAXC>
 struct __align__(1024) SmemT {
   uint8_t K[2][kKeysPerCta * 128];  // [d-half][row][128 B], 128-byte swizzle
   uint8_t Q[2][kRows * 128];
+  // key lists that fit the row-partial area beside this CTA's own sorted list
+  static constexpr int kU1Copies = MAXC * kRows / kKeysPerCta - 1;
   union {
     float2 part[2][kRows];          // pass-1 (max, sum) per column half
     unsigned long long lists[(MAXC - 2) * 32];  // cluster-level merge of the eviction candidates
+    unsigned long long copy[kKeysPerCta];       // local copy of another CTA's sorted keys
   } u0;
   union {
     float2 recv[MAXC][kRows];                   // (max, sum) partials of every CTA
     struct {
       unsigned long long key[kKeysPerCta];      // eviction keys of this CTA (sorted on the many-eviction path)
-      unsigned long long copy[kKeysPerCta];     // local copy of another CTA's sorted keys
+      unsigned long long copy[kU1Copies][kKeysPerCta];  // local copies of other CTAs' sorted keys
     } sel;
   } u1;
   unsigned long long cand_recv[MAXC * 32];  // sorted bottom-32 list of every CTA
@@ -77,7 +81,23 @@ struct __align__(1024) SmemT {
 // 1 KB alignment slack of the dynamic allocation
 static_assert(sizeof(SmemT<8>) + 1024 <= (228 * 1024 - 2 * 1024) / 2, "8-CTA clusters: two CTAs per SM");
 static_assert(sizeof(SmemT<16>) + 1024 <= 227 * 1024, "16-CTA clusters: one CTA per SM");
-static_assert(sizeof(SmemT<8>::cand_recv) >= kKeysPerCta * 8, "a copied key list fits the candidate lists");
+static_assert(sizeof(SmemT<8>::cand_recv) % (kKeysPerCta * 8) == 0, "the candidate lists hold whole key lists");
+
+// Local key-list buffers of the many-eviction selection: the row-partial area beside the
+// CTA's own list, the candidate lists and u0.  None of them is used by anything else between
+// the sort and barrier #2 on that path (the candidate lists and the u0 merge belong to the
+// few-eviction path; the row partials of the unit have been combined, and those of the next
+// unit only arrive after barrier #2).
+template <int MAXC>
+constexpr int kSelBufs = SmemT<MAXC>::kU1Copies + MAXC / 8 + 1;
+
+template <int MAXC>
+__device__ __forceinline__ unsigned long long* sel_buf(SmemT<MAXC>& s, int i) {
+  constexpr int nu1 = SmemT<MAXC>::kU1Copies, nc = MAXC / 8;
+  if (i < nu1) return s.u1.sel.copy[i];
+  if (i < nu1 + nc) return s.cand_recv + (i - nu1) * kKeysPerCta;
+  return s.u0.copy;
+}
 
 // Sorts one 64-bit key per lane ascending across the warp (bitonic network).
 __device__ __forceinline__ unsigned long long warp_sort32(unsigned long long x, int lane) {
@@ -491,66 +511,79 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
       for (int dst = 0; dst < C; ++dst) st_cluster_u64(mapa(local, dst), mine);
     }
   } else {
-    // Many evictions (the first compression after a long prefill): every CTA sorts its 256
-    // keys (bitonic network: partners within a warp by shuffles, across warps through shared
-    // memory).  After a cluster barrier every CTA copies the sorted lists of the cluster into
-    // its own shared memory (one coalesced remote load per thread and list, all issued at
-    // once), two lists at a time, and each key counts the smaller keys of each list by binary
-    // search there.
-    if (!skip) {  // uniform over the CTA
-      unsigned long long x = mykey;
-#pragma unroll
-      for (int k2 = 2; k2 <= kKeysPerCta; k2 <<= 1)
-#pragma unroll
-        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-          unsigned long long y;
-          if (j2 >= 32) {
-            lst[tid] = x;
-            __syncthreads();
-            y = lst[tid ^ j2];
-            __syncthreads();
-          } else {
-            y = __shfl_xor_sync(0xffffffffu, x, j2);
-          }
-          // the lower index of a pair keeps the smaller key in an ascending run
-          const bool keep_min = ((tid & j2) == 0) == ((tid & k2) == 0);
-          x = keep_min ? (x < y ? x : y) : (x < y ? y : x);
-        }
-      lst[tid] = x;
+    // Many evictions (the first compression after a long prefill).  Each warp sorts its 32
+    // keys; each key then takes its place in the CTA's sorted list by counting the smaller
+    // keys of the other warps' sorted runs (binary search), so the cross-warp part of the sort
+    // costs one CTA barrier.  After a cluster barrier thread i takes key i of its CTA's sorted
+    // list: i keys of its own CTA lie below it, and the smaller keys of every other CTA are
+    // counted by binary search in local copies of their sorted lists (one coalesced remote
+    // load per thread and list, all issued at once, kSelBufs lists searched per round).  The
+    // evicted keys of the CTA are the prefix of its sorted list whose ranks are below E.
+    constexpr int kWarps = kThreads / 32;
+    constexpr int NB = kSelBufs<MAXC>;
+    unsigned long long* const runs = s.u1.sel.copy[0];
+    unsigned long long xs = 0ull;
+    if (!skip) {  // uniform over the cluster
+      xs = warp_sort32(mykey, lane);
+      runs[tid] = xs;
     }
-    cluster_sync();  // every CTA's sorted list is complete
-    if (!skip) {  // uniform over the CTA
-      unsigned long long rk[MAXC];
+    __syncthreads();
+    if (!skip) {
+      int pw[kWarps - 1];
+#pragma unroll
+      for (int i = 0; i < kWarps - 1; ++i) pw[i] = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+#pragma unroll
+        for (int i = 0; i < kWarps - 1; ++i)
+          if (runs[((warp + 1 + i) % kWarps) * 32 + pw[i] + step - 1] < xs) pw[i] += step;
+      int pos = lane;
+#pragma unroll
+      for (int i = 0; i < kWarps - 1; ++i)
+        pos += pw[i] + (runs[((warp + 1 + i) % kWarps) * 32 + pw[i]] < xs ? 1 : 0);
+      lst[pos] = xs;
+    }
+    cluster_sync();  // every CTA's sorted list is complete (and this CTA's runs are read)
+    bool ev_sorted = false;
+    if (!skip) {
+      const unsigned long long x = lst[tid];
+      unsigned long long rk[MAXC - 1];  // the other CTAs' lists, starting after this one
       const uint32_t mine = smem_u32(&lst[tid]);
 #pragma unroll
-      for (int cc = 0; cc < MAXC; ++cc) rk[cc] = cc < C ? ld_cluster_u64(mapa(mine, cc)) : 0ull;
-      // local buffers: nothing else uses them on this path between the sort and barrier #2
-      // (the candidate lists belong to the few-eviction path, u0 to passes 1 and the merge)
-      unsigned long long* const buf0 = s.u1.sel.copy;
-      unsigned long long* const buf1 = s.cand_recv;
-      int rank = 0;
-#pragma unroll
-      for (int cc = 0; cc < MAXC; cc += 2) {
-        if (cc >= C) break;  // C is uniform over the cluster
-        const bool two = cc + 1 < C;
-        buf0[tid] = rk[cc];
-        if (two) buf1[tid] = rk[cc + 1];
-        __syncthreads();
-        // keys below mykey in each list: the halving steps reach 255 at most, the last
-        // compare counts the list's last key
-        int p0 = 0, p1 = 0;
-#pragma unroll
-        for (int step = kKeysPerCta / 2; step > 0; step >>= 1) {
-          if (buf0[p0 + step - 1] < mykey) p0 += step;
-          if (two && buf1[p1 + step - 1] < mykey) p1 += step;
-        }
-        p0 += buf0[p0] < mykey ? 1 : 0;
-        if (two) p1 += buf1[p1] < mykey ? 1 : 0;
-        rank += p0 + p1;
-        __syncthreads();
+      for (int i = 0; i < MAXC - 1; ++i) {
+        int cc = c + 1 + i;
+        if (cc >= C) cc -= C;
+        rk[i] = i < C - 1 ? ld_cluster_u64(mapa(mine, cc)) : 0ull;
       }
-      evicted = key_valid && rank < E;
+      int rank = tid;
+#pragma unroll
+      for (int r0 = 0; r0 < MAXC - 1; r0 += NB) {
+        if (r0 >= C - 1) break;  // C is uniform over the cluster
+        const int nr = min(NB, C - 1 - r0);
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+          if (r0 + i < MAXC - 1 && i < nr) sel_buf(s, i)[tid] = rk[r0 + i];
+        __syncthreads();
+        // keys below x in each list: the halving steps reach 255 at most, the last compare
+        // counts the list's last key
+        int p[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) p[i] = 0;
+#pragma unroll
+        for (int step = kKeysPerCta / 2; step > 0; step >>= 1)
+#pragma unroll
+          for (int i = 0; i < NB; ++i)
+            if (r0 + i < MAXC - 1 && i < nr && sel_buf(s, i)[p[i] + step - 1] < x) p[i] += step;
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+          if (r0 + i < MAXC - 1 && i < nr) rank += p[i] + (sel_buf(s, i)[p[i]] < x ? 1 : 0);
+        if (r0 + NB < C - 1) __syncthreads();  // the next round overwrites the copies
+      }
+      ev_sorted = rank < E;
     }
+    // ranks grow along the sorted list, so this CTA's evicted keys are its first m keys
+    const int m = __syncthreads_count(!skip && ev_sorted);
+    if (!skip) evicted = key_valid && (m >= kKeysPerCta || mykey < lst[m]);
     const int kept_cta = __syncthreads_count(!skip && key_valid && !evicted);
     if (!skip && tid == 0) {
       const uint32_t local = smem_u32(&s.kept_recv[c]);
