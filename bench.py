@@ -265,6 +265,9 @@ def run_ours(args):
     # sequences beyond one cluster (longer than 4096 tokens) take the multi-pass form: four
     # launches per pass (its K is read twice; the algorithmic bytes count it once)
     multipass = (batch.max_seq_len or wl.L) > 4096
+    # kernels per pass: 1, or the length grouping and one launch per cluster size when the
+    # requests' lengths differ, or the four of the multi-pass form
+    launches = zipage.zp_compress_kernel_launches(batch.params, batch.max_seq_len, batch.d_nmax is not None)
     if multipass:
         traffic = None
     out = {
@@ -280,10 +283,12 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": f"{peak_kind} (hbm_gbs burst copy)",
                      "kernel": ("long_stats/long_score/long_select/long_compact (one pass)" if multipass
-                                else "compress_kernel"),
+                                else "compress_kernel" if launches == 1
+                                else f"group_by_length_kernel + compress_kernel at {launches - 1} cluster sizes"
+                                     " (one pass)"),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "launch_ms_mean": ms, "launch_ms_min": min(times)},
-        "gpu_launches": args.steps * (4 if multipass else 1),
+        "gpu_launches": args.steps * launches,
         "clocks": clk.summary(),
     }
     if not args.no_e2e:

@@ -133,7 +133,11 @@ typedef struct zp_debug {
  *   params        host.
  *   dbg           host struct or NULL.
  *   workspace     device, >= zp_compress_workspace_size() bytes, 256-byte aligned; holds the
- *                 error word.  The call clears it before the kernel runs.
+ *                 error word (cleared by the call before any kernel runs), the unit counters,
+ *                 and the request order grouped by length that the call builds when the
+ *                 requests' lengths may need clusters of different sizes (max_seq_len above
+ *                 n_max*b, or per-request budgets): each group then runs in a launch of its
+ *                 own cluster size.  One workspace serves one call in flight at a time.
  *   stream        stream to launch on.
  * Source and destination blocks of different requests must not overlap (shared prefix
  * blocks are only read).  Returns ZP_OK once queued.
@@ -147,10 +151,19 @@ zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const
                       const zp_params* params, const zp_debug* dbg, void* workspace,
                       size_t workspace_bytes, zp_stream stream);
 
-/* Bytes of workspace zp_compress needs: the device error word and unit counter (256 bytes), plus,
- * when max_seq_len exceeds 4096, the scratch of the multi-pass form (per unit: 1 KB per 256-token
- * chunk and 16 bytes per token).  max_seq_len 0 means n_max*b. */
+/* Bytes of workspace zp_compress needs.  max_seq_len 0 means n_max*b.  Up to 4096 tokens: a
+ * 512-byte header (error word, unit counters, length groups) and 4 bytes per request (the
+ * grouped request order), rounded up to 256.  Above 4096: 256 bytes and the scratch of the
+ * multi-pass form (per unit: 1 KB per 256-token chunk and 16 bytes per token). */
 size_t zp_compress_workspace_size(const zp_params* params, int32_t num_requests, int32_t max_seq_len);
+
+/* Kernel launches one zp_compress call makes for this max_seq_len (0 means n_max*b) and
+ * budget form (per_request_budgets != 0 when meta->n_max_per_req is given): 1 when every
+ * request fits one cluster size, 1 + G when the call groups the requests by length into G
+ * cluster sizes (the grouping kernel and one launch per size, empty groups included), 4 for
+ * the multi-pass form (max_seq_len above 4096).  0 for arguments zp_compress rejects on its
+ * sizes.  Host only; launches nothing. */
+int32_t zp_compress_kernel_launches(const zp_params* params, int32_t max_seq_len, int32_t per_request_budgets);
 
 /* ---------------------------------------------------------------------------------------
  * Original (all-pairs) redundancy score — the ablation of the Lightning Redundancy Score

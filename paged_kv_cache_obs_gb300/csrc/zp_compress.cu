@@ -141,16 +141,20 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
   const int q4 = warp & 3, hh = warp >> 2;  // TMEM lane quarter, key/column half
   const int C = static_cast<int>(cluster_nctarank());
   const int c = static_cast<int>(cluster_ctarank());
-  // La: the longest sequence of the launch (cluster size, TMA/MMA shapes, row length of the
-  // global scores); L: this unit's own sequence length (all masking and selection)
-  const int La = a.L, b = a.b, d = a.d, w = a.w, Rw = a.Rw, Gq = a.Gq;
+  // La: the longest sequence of the call (row length of the global scores); Lx: the keys this
+  // launch's clusters cover (cluster size, TMA/MMA shapes; La unless the requests are grouped
+  // by length); L: this unit's own sequence length (all masking and selection)
+  const int La = a.L, Lx = a.Lc, b = a.b, d = a.d, w = a.w, Rw = a.Rw, Gq = a.Gq;
   const int bs = a.b_shift, bm = b - 1;  // b is a power of two: t / b = t >> bs, t % b = t & bm
   const int t0 = c * kKeysPerCta;
-  const int nk_l = min(kKeysPerCta, La - t0);          // keys of this CTA at the launch length
+  const int nk_l = min(kKeysPerCta, Lx - t0);          // keys of this CTA at the launch length
   const int nblk_l = (nk_l + bm) >> bs;                // blocks loaded (a partial last block whole)
   const int n_mma = (nk_l + 15) & ~15;                 // MMA N over those keys
   const int nhalf = d / 64;
-  const int num_units = a.R * a.nl * a.Hkv;
+  // the launch's requests: all of them, or one length group (positions [rbase, rbase + count)
+  // of the grouped order)
+  const int rbase = a.bucket ? a.bucket[0] : 0;
+  const int num_units = (a.bucket ? a.bucket[1] : a.R) * a.nl * a.Hkv;
   const int cluster_id = static_cast<int>(blockIdx.x) / C;  // the C CTAs of a cluster are consecutive in x
   const int num_clusters = static_cast<int>(gridDim.x) / C;
 
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
   int iter = 0;
   for (int unit = cluster_id; unit < num_units; ++iter) {
   const int h = unit % a.Hkv;
-  const int r = unit / a.Hkv / a.nl;
+  const int r = a.req_order ? a.req_order[rbase + unit / a.Hkv / a.nl] : unit / a.Hkv / a.nl;
   const int layer = a.layer0 + (unit / a.Hkv) % a.nl;
   uint8_t* const head_base = a.pool + static_cast<size_t>(layer) * static_cast<size_t>(a.num_blocks) * a.block_bytes +
                              static_cast<size_t>(h) * b * a.row_bytes;
@@ -218,17 +222,17 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
 
   // Validate the request's metadata; every CTA of the cluster sees the same values, so they
   // all take the same decision without communicating.  A request holds L cached tokens with
-  // k < L <= La (L = n_max*b at the decode trigger; more after a long prefill).
+  // k < L <= Lx (L = n_max*b at the decode trigger; more after a long prefill).
   const int L = a.seq_len[r];
   // the request's block budget (all requests share n_max unless per-request budgets are given)
   const int n_max_r = a.n_max_req ? a.n_max_req[r] : a.n_max;
   // Every table entry the launch may use is loaded now, independently of L and of the budget,
   // so that these loads overlap the two above; only the request's own entries are checked.
-  const int nblk_a = (La + bm) >> bs;  // <= max_table(MAXC) <= kThreads
+  const int nblk_a = (Lx + bm) >> bs;  // <= max_table(MAXC) <= kThreads
   const int sb = tid < nblk_a ? a.block_tables[static_cast<int64_t>(r) * a.max_blocks + tid] : 0;
   const int db = tid < a.n_max - 1 ? a.dst_tables[static_cast<int64_t>(r) * a.max_blocks + tid] : 0;
   const int k_r = (n_max_r - 1) * b;                 // tokens this request keeps per head
-  bool bad = (n_max_r < 2) || (n_max_r > a.n_max) || (k_r < w) || (L <= k_r) || (L > La) || slot < 0 ||
+  bool bad = (n_max_r < 2) || (n_max_r > a.n_max) || (k_r < w) || (L <= k_r) || (L > Lx) || slot < 0 ||
              slot >= a.num_qslots;
   if (tid < nblk_a) {
     s.src_tab[tid] = sb;
@@ -720,6 +724,69 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
   if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+// Workspace header of the fused form: the error word (int 0), the unit counter of a single
+// launch (int 1), one unit counter per length group (ints 16 + C) and one (first position,
+// request count) pair per group (ints 48 + 2C); the grouped request order follows it.
+constexpr int kWsGroupCounters = 16;
+constexpr int kWsGroups = 48;
+constexpr size_t kWsHeaderBytes = 512;
+static_assert(kWsGroups * 4 >= (kWsGroupCounters + kMaxCluster + 1) * 4, "header fields overlap");
+static_assert((kWsGroups + 2 * (kMaxCluster + 1)) * 4 <= static_cast<int>(kWsHeaderBytes), "header too small");
+
+// Groups the requests by the CTAs their length needs (C_r = ceil(L_r / 256)), so that each
+// group runs in clusters of its own size and no CTA waits through a unit with no keys.
+// A request whose length cannot be valid (L_r <= k_lo or L_r > L) goes to the largest group,
+// whose kernel reports it.  One CTA; thread i takes a contiguous run of requests, so the
+// order inside a group is the request order.
+constexpr int kPlanThreads = 256;
+__global__ void __launch_bounds__(kPlanThreads) group_by_length_kernel(const int32_t* seq_len, int R, int L, int k_lo,
+                                                                       int c_max, int32_t* ws) {
+  __shared__ int cnt[kMaxCluster + 1][kPlanThreads];
+  const int tid = threadIdx.x;
+  const int per = (R + kPlanThreads - 1) / kPlanThreads;
+  const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
+  for (int c = 0; c <= kMaxCluster; ++c) cnt[c][tid] = 0;
+  auto group_of = [&](int r) {
+    const int Lr = seq_len[r];
+    return (Lr > k_lo && Lr <= L) ? (Lr + kKeysPerCta - 1) / kKeysPerCta : c_max;
+  };
+  for (int r = r0; r < r1; ++r) ++cnt[group_of(r)][tid];
+  __syncthreads();
+  if (tid <= kMaxCluster) {
+    // positions of the groups before this one, then the runs of the threads before each thread
+    int base = 0;
+    for (int c = 0; c < tid; ++c)
+      for (int t = 0; t < kPlanThreads; ++t) base += cnt[c][t];
+    ws[kWsGroups + 2 * tid] = base;
+    int n = 0;
+    for (int t = 0; t < kPlanThreads; ++t) {
+      const int x = cnt[tid][t];
+      cnt[tid][t] = base + n;
+      n += x;
+    }
+    ws[kWsGroups + 2 * tid + 1] = n;
+    ws[kWsGroupCounters + tid] = 0;
+  }
+  __syncthreads();
+  int32_t* order = ws + kWsHeaderBytes / 4;
+  for (int r = r0; r < r1; ++r) order[cnt[group_of(r)][tid]++] = r;
+}
+
+// Cluster sizes of one call: requests whose lengths may need different cluster sizes (a launch
+// length above n_max*b, or per-request budgets) are grouped by length on the device, and each
+// group runs in a launch of its own cluster size c in [c_lo, C]; otherwise (c_lo == C) one
+// launch covers every request.  k_lo is the smallest budget a request may have.
+struct ClusterPlan {
+  int C, c_lo, k_lo;
+};
+ClusterPlan cluster_plan(int L, int k, int b, bool per_request_budgets) {
+  ClusterPlan q;
+  q.C = (L + kKeysPerCta - 1) / kKeysPerCta;
+  q.k_lo = per_request_budgets ? b : k;
+  q.c_lo = std::min(q.C, (q.k_lo + 1 + kKeysPerCta - 1) / kKeysPerCta);
+  return q;
+}
+
 }  // namespace
 
 template <int MAXC>
@@ -782,12 +849,13 @@ zp_status launch_compress(const CUtensorMap& tmK, const CUtensorMap& tmQ, const 
 
 using namespace zp;
 
-// The error word and the unit counter; sequences beyond one cluster (L > 4096) add the
-// scratch of the multi-pass form.
+// The error word and the unit counters, then the grouped request order of the fused form, or,
+// for sequences beyond one cluster (L > 4096), the scratch of the multi-pass form.
 extern "C" size_t zp_compress_workspace_size(const zp_params* p, int32_t num_requests, int32_t max_seq_len) {
   if (!p || num_requests < 0) return 0;
   const int64_t L = max_seq_len > 0 ? max_seq_len : static_cast<int64_t>(p->n_max) * p->block_size;
-  if (L <= static_cast<int64_t>(kMaxCluster) * kKeysPerCta) return 256;
+  if (L <= static_cast<int64_t>(kMaxCluster) * kKeysPerCta)
+    return kWsHeaderBytes + ((static_cast<size_t>(num_requests) * 4 + 255) & ~size_t(255));
   return 256 + compress_long_scratch_bytes(static_cast<int64_t>(num_requests) * p->num_layers * p->num_kv_heads,
                                            static_cast<int>(L));
 }
@@ -893,8 +961,35 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.protect_window = p->protect_window;
   a.causal = p->causal;
 
-  const int C = (L + kKeysPerCta - 1) / kKeysPerCta;
+  const ClusterPlan plan = cluster_plan(L, k, b, meta->n_max_per_req != nullptr);
+  const int C = plan.C, c_lo = plan.c_lo;
   if (C > kMaxCluster) return launch_compress_long(tmK, tmQ, a, static_cast<uint8_t*>(workspace) + 256, st);
   const int64_t num_units = static_cast<int64_t>(R) * nl * Hkv;
-  return C <= 8 ? launch_compress<8>(tmK, tmQ, a, C, num_units, st) : launch_compress<16>(tmK, tmQ, a, C, num_units, st);
+  a.Lc = L;
+  if (c_lo == C) return C <= 8 ? launch_compress<8>(tmK, tmQ, a, C, num_units, st)
+                               : launch_compress<16>(tmK, tmQ, a, C, num_units, st);
+  int32_t* ws = static_cast<int32_t*>(workspace);
+  group_by_length_kernel<<<1, kPlanThreads, 0, st>>>(meta->seq_len, R, L, plan.k_lo, C, ws);
+  if (cudaGetLastError() != cudaSuccess) return ZP_ERR_CUDA;
+  a.req_order = ws + kWsHeaderBytes / 4;
+  for (int c = c_lo; c <= C; ++c) {
+    CompressArgs ac = a;
+    ac.Lc = std::min(L, c * kKeysPerCta);
+    ac.work = ws + kWsGroupCounters + c;
+    ac.bucket = ws + kWsGroups + 2 * c;
+    const zp_status stc = c <= 8 ? launch_compress<8>(tmK, tmQ, ac, c, num_units, st)
+                                 : launch_compress<16>(tmK, tmQ, ac, c, num_units, st);
+    if (stc != ZP_OK) return stc;
+  }
+  return ZP_OK;
+}
+
+extern "C" int32_t zp_compress_kernel_launches(const zp_params* p, int32_t max_seq_len, int32_t per_request_budgets) {
+  if (!p || p->n_max < 2 || (p->block_size != 16 && p->block_size != 32)) return 0;
+  const int b = p->block_size, k = (p->n_max - 1) * b;
+  const int L = max_seq_len > 0 ? max_seq_len : p->n_max * b;
+  if (L <= k || L > 16384) return 0;
+  const ClusterPlan plan = cluster_plan(L, k, b, per_request_budgets != 0);
+  if (plan.C > kMaxCluster) return 4;  // statistics, scores, selection, compaction
+  return plan.c_lo == plan.C ? 1 : 1 + (plan.C - plan.c_lo + 1);
 }

@@ -31,11 +31,14 @@ struct CompressArgs {
   float* gscores;
   int32_t* err;
   int32_t* work;                    // unit counter of the persistent clusters (zeroed per launch)
+  const int32_t* req_order;         // requests grouped by length (variable-length form), or nullptr
+  const int32_t* bucket;            // (first index into req_order, request count) of this launch
   float* dbg_attn;
   float* dbg_redund;
   float* dbg_score;
   int32_t* dbg_keep;
-  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, max_blocks, num_qslots;  // L: launch length
+  int R, layers, Hq, Hkv, d, b, n_max, w, Gq, Rw, L, k, max_blocks, num_qslots;  // L: longest request
+  int Lc;                         // key extent of this launch's clusters: min(L, C*256)
   int layer0, nl;                 // the call's layers: [layer0, layer0 + nl) of the `layers`
   float alpha, beta, decay, sl2;  // sl2 = scale * log2(e)
   float inv_rw;                   // 1 / (w * G_q)

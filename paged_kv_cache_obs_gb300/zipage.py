@@ -81,6 +81,7 @@ def _sig(name, res, args):
 _sig("zp_compress", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta), _P, _I32, _P,
                            ctypes.POINTER(zp_params), ctypes.POINTER(zp_debug), _P, _SZ, _P])
 _sig("zp_compress_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
+_sig("zp_compress_kernel_launches", _I32, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_paged_decode_attn", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                     ctypes.POINTER(zp_params), _P, _SZ, _P])
 _sig("zp_paged_decode_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
@@ -176,6 +177,10 @@ def _i32_array(a):
 
 def zp_compress_workspace_size(params: dict, num_requests: int, max_seq_len: int = 0) -> int:
     return lib.zp_compress_workspace_size(ctypes.byref(make_params(params)), num_requests, max_seq_len)
+
+
+def zp_compress_kernel_launches(params: dict, max_seq_len: int = 0, per_request_budgets: bool = False) -> int:
+    return lib.zp_compress_kernel_launches(ctypes.byref(make_params(params)), max_seq_len, int(per_request_budgets))
 
 
 def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_scores, params: dict,

@@ -166,6 +166,31 @@ def test_invalid_arguments_are_rejected_without_a_gpu(zp):
     assert zp.zp_paged_decode_kernel_launches(q, 3, 0) == 0
 
 
+def test_compress_launch_plan_and_workspace_without_a_gpu(zp):
+    # The launch-count query follows the cluster sizes a call needs: 256 keys per CTA, so a
+    # request of L tokens takes ceil(L / 256) CTAs.  The Llama-3-8B decode trigger (N_max 128,
+    # b 16: L = 2048, k = 2032) is one launch; after a prefill to 2048 with N_max 64 (k = 1008)
+    # the requests need 4..8 CTAs, so the grouping kernel and 5 launches; with per-request
+    # budgets (k_r >= b) any of 1..8; beyond 4096 tokens the four multi-pass kernels.
+    p = dict(num_layers=32, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, n_max=128,
+             window=32, alpha=0.5, beta=0.5, decay=0.9, scale=0.088, protect_window=1, causal=1)
+    assert zp.zp_compress_kernel_launches(p) == 1
+    assert zp.zp_compress_kernel_launches(p, 2048) == 1
+    assert zp.zp_compress_kernel_launches(dict(p, n_max=64), 2048) == 1 + 5
+    assert zp.zp_compress_kernel_launches(dict(p, n_max=64), 1024) == 1   # L = n_max*b: one size
+    assert zp.zp_compress_kernel_launches(p, 0, per_request_budgets=True) == 1 + 8
+    assert zp.zp_compress_kernel_launches(p, 4096) == 1 + (16 - 8 + 1)
+    assert zp.zp_compress_kernel_launches(p, 8192) == 4
+    assert zp.zp_compress_kernel_launches(p, 2032) == 0                  # L <= k
+    assert zp.zp_compress_kernel_launches(p, 16385) == 0
+    assert zp.zp_compress_kernel_launches(dict(p, block_size=8)) == 0
+    # workspace: a 512-byte header and the grouped request order (4 bytes per request) up to
+    # 4096 tokens, rounded up to 256 bytes
+    assert zp.zp_compress_workspace_size(p, 64) == 512 + 256
+    assert zp.zp_compress_workspace_size(p, 65) == 512 + 512
+    assert zp.zp_compress_workspace_size(p, 0) == 512
+
+
 def test_commit_after_prefill_releases_every_block_past_n_max_minus_1(zp):
     a = zp.zp_alloc_create(64)
     try:

@@ -220,15 +220,23 @@ def test_unsupported_and_empty_calls(zp):
     batch.close()
 
 
+@pytest.mark.parametrize("path", ["one_size", "grouped"])
 @pytest.mark.parametrize("bad_len", ["no_eviction", "too_long"])
-def test_wrong_seq_len_is_reported(zp, bad_len):
+def test_wrong_seq_len_is_reported(zp, bad_len, path):
+    # "grouped": the launch length (600) is above n_max*b, so the requests are grouped by
+    # length and a request whose length is invalid must still reach a kernel that reports it
     zipage, runner = zp
-    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, n_max=8)
+    if path == "one_size":
+        wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, n_max=8)
+    else:
+        wl = synth.WORKLOADS["prefill"].scaled(num_requests=3, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                               n_max=8, prefill_max=600)
     inp = synth.make_inputs(wl, "cpu")
     pool_in = synth.bf16_bits(inp.pool)
     batch = runner.CompressionBatch(inp, "cuda")
+    La = batch.max_seq_len or wl.L
     # a request must hold more than k = (n_max-1)*b tokens and at most the launch length
-    batch.d_seq[0] = (wl.n_max - 1) * wl.block_size if bad_len == "no_eviction" else wl.L + 1
+    batch.d_seq[0] = (wl.n_max - 1) * wl.block_size if bad_len == "no_eviction" else La + 1
     batch.launch()
     assert batch.error() == zipage.ZP_ERR_BAD_TABLE
     out = synth.bf16_bits(batch.pool)
@@ -422,7 +430,7 @@ def test_random_configurations_match_oracle(zp, seed):
 BAD_KINDS = ["src_past_pool", "src_negative", "dst_past_pool", "qslot_past_slots", "qslot_negative"]
 
 
-@pytest.mark.parametrize("path", ["fused", "multipass"])
+@pytest.mark.parametrize("path", ["fused", "grouped", "multipass"])
 @pytest.mark.parametrize("kind", BAD_KINDS)
 def test_bad_metadata_skips_only_that_request(zp, kind, path):
     # request 1 carries one bad entry: the call reports ZP_ERR_BAD_TABLE, request 1's blocks and
@@ -431,6 +439,9 @@ def test_bad_metadata_skips_only_that_request(zp, kind, path):
     if path == "fused":
         wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2, num_kv_heads=2, num_q_heads=8,
                                                  n_max=16)
+    elif path == "grouped":  # k = 240, lengths up to 1000: clusters of 1 to 4 CTAs
+        wl = synth.WORKLOADS["prefill"].scaled(num_requests=2, num_layers=2, num_kv_heads=2, num_q_heads=8,
+                                               n_max=16, prefill_max=1000)
     else:
         wl = synth.WORKLOADS["prefill"].scaled(num_requests=2, num_layers=1, num_kv_heads=2, num_q_heads=8,
                                                n_max=64, prefill_max=5000)
@@ -468,4 +479,33 @@ def test_bad_metadata_skips_only_that_request(zp, kind, path):
     ndiff = parity.check_units(units, pool_in, synth.bf16_bits(inp.obs_q), gs_in, batch.tables, batch.dst_tables,
                                inp.seq_len[:2], inp.qslot, wl.params(), dbg, batch.gs.cpu().numpy(), out)
     assert ndiff <= 2
+    batch.close()
+
+
+def test_length_groups_partition_the_requests(zp):
+    # After a call whose requests need different cluster sizes, the workspace holds the
+    # grouping it ran: group c (c CTAs of 256 keys) starts at int 48 + 2c of the header with
+    # (first position, count), and the order follows the 512-byte header.  Every request is in
+    # exactly one group, the group of ceil(L/256) CTAs, in request order.
+    zipage, runner = zp
+    wl = synth.WORKLOADS["prefill"].scaled(num_requests=37, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                           n_max=16, prefill_max=2048)
+    inp = synth.make_inputs(wl, "cpu")
+    batch = runner.CompressionBatch(inp, "cuda")
+    assert zipage.zp_compress_kernel_launches(batch.params, batch.max_seq_len) == 1 + 8
+    batch.launch()
+    assert batch.error() == 0
+    torch.cuda.synchronize()
+    R = inp.num_compress
+    ws = batch.workspace.view(torch.int32).cpu().numpy()
+    order = ws[128:128 + R]
+    seen = []
+    for c in range(1, 9):
+        start, count = int(ws[48 + 2 * c]), int(ws[48 + 2 * c + 1])
+        members = order[start:start + count].tolist()
+        assert members == sorted(members)
+        for r in members:
+            assert (int(inp.seq_len[r]) + 255) // 256 == c
+        seen += members
+    assert sorted(seen) == list(range(R))
     batch.close()
