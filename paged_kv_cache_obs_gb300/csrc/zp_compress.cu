@@ -739,37 +739,60 @@ static_assert((kWsGroups + 2 * (kMaxCluster + 1)) * 4 <= static_cast<int>(kWsHea
 // whose kernel reports it.  One CTA; thread i takes a contiguous run of requests, so the
 // order inside a group is the request order.
 constexpr int kPlanThreads = 256;
+constexpr int kGroups = kMaxCluster + 1;  // group c holds requests of c CTAs (c = 0 unused)
 __global__ void __launch_bounds__(kPlanThreads) group_by_length_kernel(const int32_t* seq_len, int R, int L, int k_lo,
                                                                        int c_max, int32_t* ws) {
-  __shared__ int cnt[kMaxCluster + 1][kPlanThreads];
-  const int tid = threadIdx.x;
+  __shared__ int cnt[kGroups][kPlanThreads];  // per (group, thread): count, then first position
+  __shared__ int total[kGroups], first[kGroups];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int per = (R + kPlanThreads - 1) / kPlanThreads;
   const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
-  for (int c = 0; c <= kMaxCluster; ++c) cnt[c][tid] = 0;
+  for (int c = 0; c < kGroups; ++c) cnt[c][tid] = 0;
   auto group_of = [&](int r) {
     const int Lr = seq_len[r];
     return (Lr > k_lo && Lr <= L) ? (Lr + kKeysPerCta - 1) / kKeysPerCta : c_max;
   };
   for (int r = r0; r < r1; ++r) ++cnt[group_of(r)][tid];
   __syncthreads();
-  if (tid <= kMaxCluster) {
-    // positions of the groups before this one, then the runs of the threads before each thread
-    int base = 0;
-    for (int c = 0; c < tid; ++c)
-      for (int t = 0; t < kPlanThreads; ++t) base += cnt[c][t];
-    ws[kWsGroups + 2 * tid] = base;
-    int n = 0;
-    for (int t = 0; t < kPlanThreads; ++t) {
-      const int x = cnt[tid][t];
-      cnt[tid][t] = base + n;
-      n += x;
+  // exclusive scan over the threads, one group per warp at a time: lane l takes the 8
+  // consecutive threads 8l .. 8l + 7
+  constexpr int kPerLane = kPlanThreads / 32;
+  for (int c = warp; c < kGroups; c += kPlanThreads / 32) {
+    int v[kPerLane], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+      v[j] = cnt[c][lane * kPerLane + j];
+      sum += v[j];
     }
-    ws[kWsGroups + 2 * tid + 1] = n;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+      cnt[c][lane * kPerLane + j] = run;
+      run += v[j];
+    }
+    if (lane == 31) total[c] = incl;
+  }
+  __syncthreads();
+  if (tid < kGroups) {
+    int base = 0;
+    for (int c = 0; c < tid; ++c) base += total[c];
+    ws[kWsGroups + 2 * tid] = base;
+    ws[kWsGroups + 2 * tid + 1] = total[tid];
     ws[kWsGroupCounters + tid] = 0;
+    first[tid] = base;
   }
   __syncthreads();
   int32_t* order = ws + kWsHeaderBytes / 4;
-  for (int r = r0; r < r1; ++r) order[cnt[group_of(r)][tid]++] = r;
+  for (int r = r0; r < r1; ++r) {
+    const int c = group_of(r);
+    order[first[c] + cnt[c][tid]++] = r;
+  }
 }
 
 // Cluster sizes of one call: requests whose lengths may need different cluster sizes (a launch

@@ -482,25 +482,29 @@ def test_bad_metadata_skips_only_that_request(zp, kind, path):
     batch.close()
 
 
-def test_length_groups_partition_the_requests(zp):
+@pytest.mark.parametrize("R,n_max,prefill_max", [(37, 16, 2048), (600, 8, 600)])
+def test_length_groups_partition_the_requests(zp, R, n_max, prefill_max):
     # After a call whose requests need different cluster sizes, the workspace holds the
     # grouping it ran: group c (c CTAs of 256 keys) starts at int 48 + 2c of the header with
     # (first position, count), and the order follows the 512-byte header.  Every request is in
-    # exactly one group, the group of ceil(L/256) CTAs, in request order.
+    # exactly one group, the group of ceil(L/256) CTAs, in request order.  600 requests give
+    # the grouping kernel's threads several requests each.
     zipage, runner = zp
-    wl = synth.WORKLOADS["prefill"].scaled(num_requests=37, num_layers=1, num_kv_heads=2, num_q_heads=8,
-                                           n_max=16, prefill_max=2048)
+    wl = synth.WORKLOADS["prefill"].scaled(num_requests=R, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                           n_max=n_max, prefill_max=prefill_max)
     inp = synth.make_inputs(wl, "cpu")
     batch = runner.CompressionBatch(inp, "cuda")
-    assert zipage.zp_compress_kernel_launches(batch.params, batch.max_seq_len) == 1 + 8
+    k = (n_max - 1) * wl.block_size
+    c_lo, c_hi = (k + 1 + 255) // 256, (prefill_max + 255) // 256
+    assert zipage.zp_compress_kernel_launches(batch.params, batch.max_seq_len) == 1 + (c_hi - c_lo + 1)
     batch.launch()
     assert batch.error() == 0
     torch.cuda.synchronize()
-    R = inp.num_compress
+    assert inp.num_compress == R
     ws = batch.workspace.view(torch.int32).cpu().numpy()
     order = ws[128:128 + R]
     seen = []
-    for c in range(1, 9):
+    for c in range(c_lo, c_hi + 1):
         start, count = int(ws[48 + 2 * c]), int(ws[48 + 2 * c + 1])
         members = order[start:start + count].tolist()
         assert members == sorted(members)
