@@ -370,12 +370,18 @@ def test_timed_launch_without_debug_outputs_is_bit_identical(zp, name):
     batch.close()
 
 
-def test_layer_by_layer_equals_one_call(zp):
+@pytest.mark.parametrize("grouped", [False, True])
+def test_layer_by_layer_equals_one_call(zp, grouped):
     """Compressing the layers one call at a time, in any order, gives the same bytes as one
     call over every layer (units are independent; the one-call pass is checked against the
-    oracle by the tests above)."""
+    oracle by the tests above).  "grouped": requests of different lengths after a prefill, so
+    every call groups them by cluster size again."""
     zipage, runner = zp
-    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=4)
+    if grouped:
+        wl = synth.WORKLOADS["prefill"].scaled(num_requests=5, num_layers=4, num_kv_heads=2, num_q_heads=8,
+                                               n_max=16, prefill_max=1500)
+    else:
+        wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=4)
     inp = synth.make_inputs(wl, "cpu", seed=77)
     whole = runner.CompressionBatch(inp, "cuda")
     whole.launch()
