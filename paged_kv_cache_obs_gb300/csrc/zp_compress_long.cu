@@ -73,19 +73,26 @@ __device__ __forceinline__ UnitMeta unit_meta(const CompressArgs& a, int unit) {
 constexpr int kChunksPerCta = 16;
 constexpr int kGroupBlocks = kChunksPerCta * kKeysPerCta / 16;  // block ids of a group (b >= 16)
 
-// TMA of one chunk's K blocks (tid 0); the first chunk of a CTA also brings the window queries.
+// TMA of one chunk's K blocks by the 32 lanes of one warp (called by all of them): lane 0
+// registers the bytes (and, for the first chunk of a CTA, brings the window queries), then lane
+// i issues the boxes of blocks i, i + 32, ...  One thread issuing all of a chunk's 32 boxes in
+// sequence stalled its warp for about 6.8k cycles; lanes issuing at once take a fraction of that.
 __device__ __forceinline__ void issue_chunk_tma(LongSmem& s, const CUtensorMap* tmK, const CUtensorMap* tmQ,
                                                 const CompressArgs& a, const UnitMeta& m, const int* phys, int nblk,
-                                                bool with_q) {
+                                                bool with_q, int lane) {
   const int nhalf = a.d / 64;
-  mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>(((nblk << a.b_shift) + (with_q ? a.Rw : 0)) * a.d * 2));
-  if (with_q)
-    for (int hd = 0; hd < nhalf; ++hd)
-      tma_load_3d(&s.Q[hd][0], tmQ, &s.bar_tma, hd * 64, m.h * a.Gq, (m.slot * a.layers + m.layer) * a.w);
-  for (int bi = 0; bi < nblk; ++bi)
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>(((nblk << a.b_shift) + (with_q ? a.Rw : 0)) * a.d * 2));
+    if (with_q)
+      for (int hd = 0; hd < nhalf; ++hd)
+        tma_load_3d(&s.Q[hd][0], tmQ, &s.bar_tma, hd * 64, m.h * a.Gq, (m.slot * a.layers + m.layer) * a.w);
+  }
+  __syncwarp();
+  for (int bi = lane; bi < nblk; bi += 32)
     for (int hd = 0; hd < nhalf; ++hd)
       tma_load_3d(&s.K[hd][bi * a.b * 128], tmK, &s.bar_tma, hd * 64, m.h * a.b,
                   m.layer * static_cast<int>(a.num_blocks) + phys[bi]);
+  __syncwarp();
 }
 
 // Chunks [c0, c1) of the unit that this CTA takes (c1 <= c0: none).
@@ -158,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tbase = s.tmem_base;
   bool ok = true, tma_pending = false;  // (tid 0)
   uint32_t ph_tma = 0, ph_mma = 0;
-  if (tid == 0) {
-    issue_chunk_tma(s, &tmK, &tmQ, a, m, phys, (chunk_keys(m, c0) + a.b - 1) >> a.b_shift, true);
-    tma_pending = true;
+  if (warp == 0) {
+    issue_chunk_tma(s, &tmK, &tmQ, a, m, phys, (chunk_keys(m, c0) + a.b - 1) >> a.b_shift, true, lane);
+    tma_pending = true;  // (meaningful in tid 0)
   }
   bool fail = false;
   int boff = 0;  // the chunk's first entry in phys
@@ -201,9 +208,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     fail = __syncthreads_or(!ok);
     tc_fence_after();
     if (fail) break;
-    if (tid == 0 && c + 1 < c1) {
-      issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false);
-      tma_pending = true;
+    if (warp == 0 && c + 1 < c1) {
+      issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false,
+                      lane);
+      tma_pending = true;  // (meaningful in tid 0)
     }
     boff += nblk;
     {
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   LongSmem& s = *reinterpret_cast<LongSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ int phys[kGroupBlocks];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, hh = warp >> 2;
   const int unit = static_cast<int>(blockIdx.x) / sc.ngrp, g = static_cast<int>(blockIdx.x) % sc.ngrp;
   const UnitMeta m = unit_meta(a, unit);
@@ -293,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tbase = s.tmem_base;
   bool ok = true, tma_pending = false;  // (tid 0)
   uint32_t ph_tma = 0, ph_mma = 0;
-  if (tid == 0) {
-    issue_chunk_tma(s, &tmK, &tmQ, a, m, phys, (chunk_keys(m, c0) + a.b - 1) >> a.b_shift, true);
-    tma_pending = true;
+  if (warp == 0) {
+    issue_chunk_tma(s, &tmK, &tmQ, a, m, phys, (chunk_keys(m, c0) + a.b - 1) >> a.b_shift, true, lane);
+    tma_pending = true;  // (meaningful in tid 0)
   }
   const int64_t gbase = ((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
   const int64_t dbase = ((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
@@ -323,12 +331,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_commit(&s.bar_mma);
         ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs);
         ph_mma ^= 1;
-        // the MMA has read K: the next chunk's copy may land while pass 2 runs
-        if (ok && c + 1 < c1) {
-          issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false);
-          tma_pending = true;
-        }
       }
+    }
+    // the MMA has read K: warp 0 issues the next chunk's copy, which lands while pass 2 runs
+    if (warp == 0 && c + 1 < c1 && __shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+      issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false,
+                      lane);
+      tma_pending = true;  // (meaningful in tid 0)
     }
     fail = __syncthreads_or(!ok);
     tc_fence_after();
