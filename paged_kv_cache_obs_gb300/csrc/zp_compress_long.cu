@@ -95,6 +95,21 @@ __device__ __forceinline__ void issue_chunk_tma(LongSmem& s, const CUtensorMap* 
   __syncwarp();
 }
 
+// The K boxes of a chunk whose rows fall in warp `warp`'s 32 rows of the tile (blocks
+// [32 warp / b, 32 (warp + 1) / b) of the chunk's nblk), one box per lane, on the already armed
+// bar_tma.  Called by all 32 lanes of the warp.
+__device__ __forceinline__ void issue_warp_boxes(LongSmem& s, const CUtensorMap* tmK, const CompressArgs& a,
+                                                 const UnitMeta& m, const int* phys, int nblk, int warp, int lane) {
+  const int nhalf = a.d / 64;
+  const int b0 = (warp * 32) >> a.b_shift, b1 = min(nblk, ((warp + 1) * 32) >> a.b_shift);
+  if (lane < (b1 - b0) * nhalf) {
+    const int bi = b0 + lane / nhalf, hd = lane % nhalf;
+    tma_load_3d(&s.K[hd][bi * a.b * 128], tmK, &s.bar_tma, hd * 64, m.h * a.b,
+                m.layer * static_cast<int>(a.num_blocks) + phys[bi]);
+  }
+  __syncwarp();
+}
+
 // Chunks [c0, c1) of the unit that this CTA takes (c1 <= c0: none).
 __device__ __forceinline__ void group_range(const LongScratch& sc, const UnitMeta& m, int g, int& c0, int& c1) {
   c0 = g * kChunksPerCta;
@@ -175,11 +190,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int t0 = c * kKeysPerCta;
     const int nk = chunk_keys(m, c);
     const int nblk = (nk + a.b - 1) >> a.b_shift;
+    const int nblk_next = c + 1 < c1 ? (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift : 0;
     if (tid == 0) {
       ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
       if (ok) {
         ph_tma ^= 1;
         tma_pending = false;
+        if (nblk_next > 0) {  // the next chunk's copy; its boxes come from the warps below
+          mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nblk_next << a.b_shift) * a.d * 2));
+          tma_pending = true;
+        }
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, (nk + 15) & ~15);
         for (int kk = 0; kk < a.d / 16; ++kk)
@@ -199,20 +219,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (a.dbg_redund) a.dbg_redund[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t0 + tid] = red;
       }
     }
-    if (tid == 0) {
-      ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs);
-      ph_mma ^= 1;
-    }
-    // every read of K (the MMA and the redundancy) precedes the next chunk's TMA
-    fence_proxy_async_smem();
-    fail = __syncthreads_or(!ok);
+    // This warp's K rows are read (the redundancy); once D1, which reads every row, has
+    // completed, they take the next chunk's blocks.  No CTA barrier: each warp issues its own
+    // boxes and goes on to pass 1.
+    const bool wok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs);
+    ph_mma ^= 1;
     tc_fence_after();
-    if (fail) break;
-    if (warp == 0 && c + 1 < c1) {
-      issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false,
-                      lane);
-      tma_pending = true;  // (meaningful in tid 0)
+    if (__all_sync(0xffffffffu, wok) && nblk_next > 0) {
+      fence_proxy_async_smem();  // this warp's generic reads of K before the copies that replace it
+      __syncwarp();
+      issue_warp_boxes(s, &tmK, a, m, phys + boff + nblk, nblk_next, warp, lane);
     }
+    ok = ok && wok;
     boff += nblk;
     {
       // pass 1: thread = window row i, warp half hh = 128 key columns; keys t <= L-w+i/G_q
@@ -240,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // every TMEM read of D1 precedes the next chunk's MMA
     tc_fence_before();
-    __syncthreads();
+    fail = __syncthreads_or(!ok);
+    if (fail) break;
     if (tid < kRows) {
       const float2 p0 = s.part[0][tid], p1 = s.part[1][tid];
       float mm = fmaxf(p0.x, p1.x), l = 0.0f;
@@ -317,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the global score and redundancy of this thread's key load while the chunk's copy runs
     const float g_in = tid < nk ? a.gscores[gbase + kt] : 0.0f;
     const float r_in = tid < nk ? sc.red[static_cast<int64_t>(unit) * a.L + kt] : 0.0f;
+    const int nblk_next = c + 1 < c1 ? (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift : 0;
     if (tid == 0) {
       ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
       if (ok) {
@@ -331,17 +351,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_commit(&s.bar_mma);
         ok = mbar_wait_bounded(&s.bar_mma, ph_mma, kWaitNs);
         ph_mma ^= 1;
+        if (ok && nblk_next > 0) {  // the next chunk's copy; its boxes come from every warp below
+          mbar_arrive_expect_tx(&s.bar_tma, static_cast<uint32_t>((nblk_next << a.b_shift) * a.d * 2));
+          tma_pending = true;
+        }
       }
     }
-    // the MMA has read K: warp 0 issues the next chunk's copy, which lands while pass 2 runs
-    if (warp == 0 && c + 1 < c1 && __shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-      issue_chunk_tma(s, &tmK, &tmQ, a, m, phys + boff + nblk, (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift, false,
-                      lane);
-      tma_pending = true;  // (meaningful in tid 0)
-    }
-    fail = __syncthreads_or(!ok);
+    fail = __syncthreads_or(!ok);  // D2 has read K (the only reader in this kernel)
     tc_fence_after();
     if (fail) break;
+    // each warp issues the next chunk's boxes for its 32 rows; they land while pass 2 runs
+    if (nblk_next > 0) issue_warp_boxes(s, &tmK, a, m, phys + boff + nblk, nblk_next, warp, lane);
     boff += nblk;
     const int wcol = hh * 128 + q4 * 32;
     float attn = 0.0f;
