@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const CompressArgs a, const LongScratch sc) {
   constexpr int kPer = kMaxLongL / kSelThreads;  // keys per thread (contiguous positions)
   __shared__ unsigned hist[256];
-  __shared__ unsigned long long sh_prefix;
-  __shared__ unsigned sh_rank;
+  __shared__ unsigned long long sh_prefix, sh_key;
+  __shared__ unsigned sh_rank, sh_count;
   __shared__ int warp_sum[kSelThreads / 32];
   __shared__ int bad_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -436,9 +436,11 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   const int L = m.L, E = L - m.k_r;
   const float* S = sc.score + static_cast<int64_t>(unit) * a.L;
   const int p0 = tid * kPer;  // this thread's positions [p0, p0 + kPer) for the destinations
-  // radix select of the E-th smallest key, 8 bits at a time from the top.  The passes read the
-  // scores from registers, loaded once with positions tid + e * kSelThreads (coalesced, every
-  // thread busy).  (Aggregating each warp's adds per distinct bin with a match was slower.)
+  // radix select of the E-th smallest key, 8 bits at a time from the top, until the chosen bin
+  // holds a single key (with distinct scores, after 2 or 3 of the 8 passes).  The passes read
+  // the scores from registers, loaded once with positions tid + e * kSelThreads (coalesced,
+  // every thread busy).  (Aggregating each warp's adds per distinct bin with a match was
+  // slower.)
   float sv[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
@@ -479,12 +481,26 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
         while (before + c[q] < rank) ++q;
         sh_prefix = prefix | (static_cast<unsigned long long>(lane * 8 + q) << shift);
         sh_rank = rank - (before + (q ? c[q - 1] : 0u));
+        sh_count = c[q] - (q ? c[q - 1] : 0u);  // keys in the chosen bin
       }
     }
     __syncthreads();
     prefix = sh_prefix;
     rank = sh_rank;
     mask |= 0xFFull << shift;
+    if (sh_count == 1) {  // uniform over the CTA
+      // one key left in the bin: it is the rank-th (rank is 1), whatever its lower bits
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const int t = tid + e * kSelThreads;
+        if (e * kSelThreads >= L) break;  // uniform over the CTA
+        const unsigned long long key = evict_key(sv[e], t);
+        if (t < L && (key & mask) == prefix) sh_key = key;
+      }
+      __syncthreads();
+      prefix = sh_key;
+      break;
+    }
   }
   const unsigned long long T = prefix;  // exactly E keys are <= T (keys are distinct)
   // destinations: j = number of kept keys before t
