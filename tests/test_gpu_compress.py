@@ -113,11 +113,18 @@ def test_compress_matches_oracle_every_unit(zp, name):
     assert ndiff <= 2
 
 
-def test_exact_ties_keep_the_earlier_tokens(zp):
+@pytest.mark.parametrize("path", ["trigger", "many_evictions", "multipass"])
+def test_exact_ties_keep_the_earlier_tokens(zp, path):
     # all keys of a head identical, no global score, alpha = beta = 0, non-causal: every
-    # unprotected token has the same score, so the earliest k tokens are kept.
-    wl = synth.WORKLOADS["llama3_8b"].scaled(num_requests=1, num_layers=1, n_max=24, alpha=0.0,
-                                             beta=0.0, causal=0, protect_window=0)
+    # unprotected token has the same score, so the earliest k tokens are kept.  The paths:
+    # E = b at the decode trigger; E up to 632 after a prefill (ranks across the cluster);
+    # a launch length past 4096 (radix select, which must resolve the ties by position).
+    kw = dict(num_requests=1, num_layers=1, n_max=24, alpha=0.0, beta=0.0, causal=0, protect_window=0)
+    if path == "trigger":
+        wl = synth.WORKLOADS["llama3_8b"].scaled(**kw)
+    else:
+        wl = synth.WORKLOADS["prefill"].scaled(num_kv_heads=2, num_q_heads=8,
+                                               prefill_max=1000 if path == "many_evictions" else 5000, **kw)
 
     def mutate(inp):
         inp.pool[:, :, 0] = inp.pool[:, :1, 0, :, :1]
