@@ -395,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
   }
   const int wcol = hh * 128 + q4 * 32;  // first key of this warp (TMEM lanes of pass 2)
   if (!skip && warp * 32 < nk) {
-    red = (b == 16) ? warp_lightning_redundancy<16>(s.K, s.inv_n, warp * 32, lane, d, t0, L)
-                    : warp_lightning_redundancy<32>(s.K, s.inv_n, warp * 32, lane, d, t0, L);
+    red = (b == 16) ? warp_lightning_redundancy_rolled<16>(s.K, s.inv_n, warp * 32, lane, d, t0, L)
+                    : warp_lightning_redundancy_rolled<32>(s.K, s.inv_n, warp * 32, lane, d, t0, L);
   }
 
   if (!skip) {

@@ -83,14 +83,18 @@ __device__ __forceinline__ size_t row_off_bytes(const CompressArgs& a, int phys,
          static_cast<uint32_t>(row) * a.row_bytes;
 }
 
-// Lightning redundancy of the 32 keys [key0, key0 + 32) of one warp (BW = block size 16 or 32),
-// from K in 128-byte-swizzled shared memory, with warp-level mma.sync: the BW x BW Gram of each
-// block (G = K K^T, so one ldmatrix per k-step gives both the A and the B fragments), squared
-// norms from its diagonal, and the in-block row sums of cos(k_t, k_j), j != t, over the tokens
-// the block holds (keys at or past L are excluded).  Returns the redundancy of key key0 + lane.
-template <int BW>
-__device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2][kKeysPerCta * 128], float* inv_n,
-                                                           int key0, int lane, int d, int t0, int L) {
+// Lightning redundancy of the 32 keys [key0, key0 + 32) of one warp (BW = block size 16 or 32;
+// KS = d / 16 k-steps, unrolled, or KS = 0: a loop over the d / 16 k-steps, which keeps fewer
+// registers live), from K in 128-byte-swizzled shared memory, with warp-level mma.sync:
+// the BW x BW Gram of each block (G = K K^T, so one ldmatrix per k-step gives both the A and the
+// B fragments), squared norms from its diagonal, and the in-block row sums of cos(k_t, k_j),
+// j != t, over the tokens the block holds (keys at or past L are excluded).  Returns the
+// redundancy of key key0 + lane.  The unrolled form takes reciprocal norms by rsqrt (clamped
+// like 1 / max(norm, 1e-12)) and divides the mean with the fast reciprocal, both within a few
+// ulp of the loop form's IEEE square root and divisions.
+template <int BW, int KS>
+__device__ __forceinline__ float lightning_redundancy_ks(const uint8_t (&K)[2][kKeysPerCta * 128], float* inv_n,
+                                                         int key0, int lane, int d, int t0, int L) {
   constexpr int NT = BW / 8;  // n8 tiles per m16 row tile
   float acc[2][NT][4];
 #pragma unroll
@@ -99,24 +103,32 @@ __device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2]
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
-  for (int ks = 0; ks < (d >> 4); ++ks) {
-    uint32_t f[2][4];
+  // The k-steps: with KS > 0 the outer loop is unrolled KS times and the inner one runs once;
+  // with KS = 0 the outer one runs once and the inner one loops over d / 16 (the code the
+  // compiler generates for that form is the one the register budget of the fused kernel was
+  // set with).  A k-step loads both m-tiles' fragments by ldmatrix, then runs the block Gram
+  // MMAs.
+  const int nks = KS > 0 ? KS : (d >> 4);
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int row = key0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int chunk = 2 * ks + (lane >> 4);
-      ldmatrix_x4(smem_u32(&K[chunk >> 3][row * 128 + (((chunk & 7) ^ (row & 7)) << 4)]), f[mt]);
-    }
+  for (int ks = 0; ks < (KS > 0 ? KS : 1); ++ks)
+    for (int ks2 = ks; ks2 < nks; ks2 += (KS > 0 ? nks : 1)) {
+      uint32_t f[2][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        // columns 8nt..8nt+7 of the block: rows (sub = nt&1) of m-tile src of the same fragments
-        const int src = (BW == 16) ? mt : (nt >> 1);
-        const int sub = nt & 1;
-        mma_16816_bf16(acc[mt][nt], f[mt], sub ? f[src][1] : f[src][0], sub ? f[src][3] : f[src][2]);
+      for (int mt = 0; mt < 2; ++mt) {
+        const int row = key0 + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chunk = 2 * ks2 + (lane >> 4);
+        ldmatrix_x4(smem_u32(&K[chunk >> 3][row * 128 + (((chunk & 7) ^ (row & 7)) << 4)]), f[mt]);
       }
-  }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          // columns 8nt..8nt+7 of the block: rows (sub = nt&1) of m-tile src of the same fragments
+          const int src = (BW == 16) ? mt : (nt >> 1);
+          const int sub = nt & 1;
+          mma_16816_bf16(acc[mt][nt], f[mt], sub ? f[src][1] : f[src][0], sub ? f[src][3] : f[src][2]);
+        }
+    }
   const int g = lane >> 2, tq = lane & 3;
   // squared norms from the diagonal -> reciprocal norms in shared memory
 #pragma unroll
@@ -127,7 +139,12 @@ __device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2]
       for (int e = 0; e < 4; ++e) {
         const int row = 16 * mt + g + 8 * (e >> 1);
         const int col = (BW == 16 ? 16 * mt : 0) + 8 * nt + 2 * tq + (e & 1);
-        if (row == col) inv_n[key0 + row] = 1.0f / fmaxf(sqrtf(fmaxf(acc[mt][nt][e], 0.0f)), 1e-12f);
+        if (row == col) {
+          if constexpr (KS > 0)
+            inv_n[key0 + row] = fminf(rsqrtf(fmaxf(acc[mt][nt][e], 0.0f)), 1e12f);
+          else
+            inv_n[key0 + row] = 1.0f / fmaxf(sqrtf(fmaxf(acc[mt][nt][e], 0.0f)), 1e-12f);
+        }
       }
   __syncwarp();
   float rr[2][2];  // redundancy of rows 16mt + 8hf + g
@@ -149,7 +166,10 @@ __device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2]
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       const int bstart = (BW == 16) ? 16 * mt : 0;             // block of this row within the warp
       const int m = min(BW, L - (t0 + key0 + bstart));         // tokens the block holds
-      rr[mt][hf] = m > 1 ? sum * inv_n[key0 + row] / static_cast<float>(m - 1) : 0.0f;
+      if constexpr (KS > 0)
+        rr[mt][hf] = m > 1 ? __fdividef(sum * inv_n[key0 + row], static_cast<float>(m - 1)) : 0.0f;
+      else
+        rr[mt][hf] = m > 1 ? sum * inv_n[key0 + row] / static_cast<float>(m - 1) : 0.0f;
     }
   // deliver: lane k takes row k, computed by lane 4 * (k % 8)
   const int srcl = 4 * (lane & 7);
@@ -157,6 +177,22 @@ __device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2]
   const float v10 = __shfl_sync(0xffffffffu, rr[1][0], srcl), v11 = __shfl_sync(0xffffffffu, rr[1][1], srcl);
   const int mt = lane >> 4, hf = (lane >> 3) & 1;
   return mt ? (hf ? v11 : v10) : (hf ? v01 : v00);
+}
+
+// Unrolled for d = 128 and d = 64 (twice the code, about half the latency of the loop).
+template <int BW>
+__device__ __forceinline__ float warp_lightning_redundancy(const uint8_t (&K)[2][kKeysPerCta * 128], float* inv_n,
+                                                           int key0, int lane, int d, int t0, int L) {
+  return d == 128 ? lightning_redundancy_ks<BW, 8>(K, inv_n, key0, lane, d, t0, L)
+                  : lightning_redundancy_ks<BW, 4>(K, inv_n, key0, lane, d, t0, L);
+}
+
+// The loop form, for a kernel whose registers are already tight.
+template <int BW>
+__device__ __forceinline__ float warp_lightning_redundancy_rolled(const uint8_t (&K)[2][kKeysPerCta * 128],
+                                                                  float* inv_n, int key0, int lane, int d, int t0,
+                                                                  int L) {
+  return lightning_redundancy_ks<BW, 0>(K, inv_n, key0, lane, d, t0, L);
 }
 
 
