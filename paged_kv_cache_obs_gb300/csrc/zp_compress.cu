@@ -302,65 +302,8 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
     const int vlim = max(0, min(ncol, (a.causal ? (L - w + i / Gq) : (L - 1)) - t0 - cbase + 1));
     const int vall = max(0, min(ncol, (a.causal ? (L - w) : (L - 1)) - t0 - cbase + 1));
     const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
-    // online over two 64-column chunks: the chunk's max, then its exponentials against the
-    // running max (the sum so far is rescaled when the max grows); one TMEM read per chunk
-    float m = -INFINITY;
-    float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col0 = c2 * 64;
-      if (col0 >= ncol) break;
-      uint32_t ra[32], rb[32];
-      tmem_ld32_issue(tl + col0, ra);
-      tmem_ld32_issue(tl + col0 + 32, rb);
-      tmem_wait_ld(ra);
-      tmem_ld_dep(rb);
-      const bool fa = col0 + 32 <= vall, fb = col0 + 64 <= vall;  // groups every row sees whole
-      const int la = vlim - col0, lb = vlim - col0 - 32;          // visible columns of each group
-      float mx[4] = {m, m, m, m};
-      if (fa) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < la) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
-      }
-      if (fb) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < lb) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
-      }
-      const float mn = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      if (mn == -INFINITY) continue;  // nothing visible yet
-      if (m != -INFINITY && mn > m) {
-        const float corr = ex2((m - mn) * a.sl2);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) ls[e] *= corr;
-      }
-      m = mn;
-      const float mo = m * a.sl2;
-      if (fa) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < la) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), a.sl2, -mo));
-      }
-      if (fb) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < lb) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), a.sl2, -mo));
-      }
-    }
-    // rows without a visible key keep m = -inf and l = 0; padding rows are dropped below
-    s.u0.part[hh][i] = make_float2(m, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+    // rows without a visible key get m = -inf and l = 0; padding rows are dropped below
+    s.u0.part[hh][i] = row_stats_half(tl, ncol, vlim, vall, a.sl2);
   }
   tc_fence_before();
   __syncthreads();
@@ -446,29 +389,7 @@ __global__ void __launch_bounds__(kThreads, MAXC <= 8 ? 2 : 1)
       const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128;
       const bool all_rows = !a.causal || (t0 + wcol + 31 <= L - w);
       const int imin = a.causal ? max(0, Gq * (kt - (L - w))) : 0;
-      const float4* off4 = reinterpret_cast<const float4*>(s.row_off);
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      for (int c2 = 0; c2 < 2; ++c2) {
-        if (c2 * 64 >= Rw) break;
-        uint32_t ra[32], rb[32];
-        tmem_ld32_issue(tl + c2 * 64, ra);
-        tmem_ld32_issue(tl + c2 * 64 + 32, rb);
-        tmem_wait_ld(ra);
-        tmem_ld_dep(rb);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 o = off4[c2 * 16 + q];
-          const float oo[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int jj = 4 * q + e;  // 0..63 within this pair of loads
-            const float v = __uint_as_float(jj < 32 ? ra[jj & 31] : rb[jj & 31]);
-            const float p = ex2(fmaf(v, a.sl2, -oo[e]));
-            if (all_rows || c2 * 64 + jj >= imin) acc[e] += p;
-          }
-        }
-      }
-      attn = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * a.inv_rw;
+      attn = key_mass(tl, Rw, all_rows, imin, s.row_off, a.sl2) * a.inv_rw;
     }
     S = (attn + a.alpha * g_in) - a.beta * red;
     if (a.protect_window && kt >= L - w) S = INFINITY;

@@ -83,6 +83,105 @@ __device__ __forceinline__ size_t row_off_bytes(const CompressArgs& a, int phys,
          static_cast<uint32_t>(row) * a.row_bytes;
 }
 
+// Pass 1 of one window row over one 128-column half of a 256-key tile of scores in TMEM (row =
+// this thread's TMEM lane, columns from `tl`): the row's max and its exp2-sum relative to that
+// max, over the scaled scores (scale sl2) of columns [0, ncol), of which [0, vlim) are visible to
+// this row and [0, vall) to every row.  Online over two 64-column chunks: the chunk's max, then
+// its exponentials against the running max (the sum so far is rescaled when the max grows);
+// two 32-column loads per wait and four partial sums.  A group of 32 columns that every row
+// sees whole takes the unpredicated path; the others compare each column with this row's limit.
+// A row with no visible column gives (-inf, 0).
+__device__ __forceinline__ float2 row_stats_half(uint32_t tl, int ncol, int vlim, int vall, float sl2) {
+  float m = -INFINITY;
+  float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int c2 = 0; c2 < 2; ++c2) {
+    const int col0 = c2 * 64;
+    if (col0 >= ncol) break;
+    uint32_t ra[32], rb[32];
+    tmem_ld32_issue(tl + col0, ra);
+    tmem_ld32_issue(tl + col0 + 32, rb);
+    tmem_wait_ld(ra);
+    tmem_ld_dep(rb);
+    const bool fa = col0 + 32 <= vall, fb = col0 + 64 <= vall;  // groups every row sees whole
+    const int la = vlim - col0, lb = vlim - col0 - 32;          // visible columns of each group
+    float mx[4] = {m, m, m, m};
+    if (fa) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < la) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(ra[j]));
+    }
+    if (fb) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < lb) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(rb[j]));
+    }
+    const float mn = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    if (mn == -INFINITY) continue;  // nothing visible yet
+    if (m != -INFINITY && mn > m) {
+      const float corr = ex2((m - mn) * sl2);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ls[e] *= corr;
+    }
+    m = mn;
+    const float mo = m * sl2;
+    if (fa) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), sl2, -mo));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < la) ls[j & 3] += ex2(fmaf(__uint_as_float(ra[j]), sl2, -mo));
+    }
+    if (fb) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), sl2, -mo));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < lb) ls[j & 3] += ex2(fmaf(__uint_as_float(rb[j]), sl2, -mo));
+    }
+  }
+  return make_float2(m, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+}
+
+// Pass 2 for one key over the window rows of a score tile in TMEM (key = this thread's TMEM
+// lane, rows as columns from `tl`): the sum over the rows i < Rw that see the key (i >= imin, or
+// every row when all_rows) of exp2(s_i * sl2 - row_off[i]), row_off[i] being row i's log2
+// normaliser in scaled units (+inf for padding rows, which add 0).  Two 32-column loads per
+// wait, four partial sums; row_off is read as float4 (16-byte aligned).
+__device__ __forceinline__ float key_mass(uint32_t tl, int Rw, bool all_rows, int imin, const float* row_off,
+                                          float sl2) {
+  const float4* off4 = reinterpret_cast<const float4*>(row_off);
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int c2 = 0; c2 < 2; ++c2) {
+    if (c2 * 64 >= Rw) break;
+    uint32_t ra[32], rb[32];
+    tmem_ld32_issue(tl + c2 * 64, ra);
+    tmem_ld32_issue(tl + c2 * 64 + 32, rb);
+    tmem_wait_ld(ra);
+    tmem_ld_dep(rb);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float4 o = off4[c2 * 16 + q];
+      const float oo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int jj = 4 * q + e;  // 0..63 within this pair of loads
+        const float v = __uint_as_float(jj < 32 ? ra[jj & 31] : rb[jj & 31]);
+        const float p = ex2(fmaf(v, sl2, -oo[e]));
+        if (all_rows || c2 * 64 + jj >= imin) acc[e] += p;
+      }
+    }
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // Lightning redundancy of the 32 keys [key0, key0 + 32) of one warp (BW = block size 16 or 32;
 // KS = d / 16 k-steps, unrolled, or KS = 0: a loop over the d / 16 k-steps, which keeps fewer
 // registers live), from K in 128-byte-swizzled shared memory, with warp-level mma.sync:

@@ -234,27 +234,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     boff += nblk;
     {
       // pass 1: thread = window row i, warp half hh = 128 key columns; keys t <= L-w+i/G_q
-      // are visible
+      // are visible (columns [0, vlim) of this half to this row, [0, vall) to every row)
       const int i = q4 * 32 + lane;
       const int cbase = hh * 128, ncol = nk - cbase;
       const int vlim = max(0, min(ncol, (a.causal ? (m.L - a.w + i / a.Gq) : (m.L - 1)) - t0 - cbase + 1));
+      const int vall = max(0, min(ncol, (a.causal ? (m.L - a.w) : (m.L - 1)) - t0 - cbase + 1));
       const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + cbase;
-      float mx = -INFINITY, ls = 0.0f;
-      for (int c2 = 0; c2 < 4 && c2 * 32 < ncol; ++c2) {
-        float v[32];
-        tmem_ld32(tl + c2 * 32, v);
-        float cm = mx;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c2 * 32 + j < vlim) cm = fmaxf(cm, v[j]);
-        if (cm == -INFINITY) continue;
-        if (mx != -INFINITY && cm > mx) ls *= ex2((mx - cm) * a.sl2);
-        mx = cm;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c2 * 32 + j < vlim) ls += ex2(fmaf(v[j], a.sl2, -mx * a.sl2));
-      }
-      s.part[hh][i] = make_float2(mx, ls);
+      s.part[hh][i] = row_stats_half(tl, ncol, vlim, vall, a.sl2);
     }
     // every TMEM read of D1 precedes the next chunk's MMA
     tc_fence_before();
@@ -367,20 +353,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     float attn = 0.0f;
     if (wcol < nk) {
       // thread = key (TMEM lane), columns = window rows; row i sees key kt iff kt <= L-w+i/G_q
+      // (every row sees every key of the warp when its last key is at most L - w)
       const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 128;
+      const bool all_rows = !a.causal || (t0 + wcol + 31 <= m.L - a.w);
       const int imin = a.causal ? max(0, a.Gq * (kt - (m.L - a.w))) : 0;
-      float acc = 0.0f;
-      for (int c2 = 0; c2 < 4 && c2 * 32 < a.Rw; ++c2) {
-        float v[32];
-        tmem_ld32(tl + c2 * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int row = c2 * 32 + j;
-          const float p = ex2(fmaf(v[j], a.sl2, -s.row_off[row]));
-          if (row >= imin) acc += p;
-        }
-      }
-      attn = acc * a.inv_rw;
+      attn = key_mass(tl, a.Rw, all_rows, imin, s.row_off, a.sl2) * a.inv_rw;
     }
     if (tid < nk) {
       const int64_t o = static_cast<int64_t>(unit) * a.L + kt;
