@@ -189,6 +189,23 @@ def test_compress_launch_plan_and_workspace_without_a_gpu(zp):
     assert zp.zp_compress_workspace_size(p, 64) == 512 + 256
     assert zp.zp_compress_workspace_size(p, 65) == 512 + 512
     assert zp.zp_compress_workspace_size(p, 0) == 512
+    # a call whose workspace is below that size is refused before anything reaches the device
+    # (the buffers below are host memory that the call must not touch)
+    import ctypes
+    import numpy as np
+    R = 64
+    host = np.zeros(1 << 16, np.uint8)
+    ptr = host.ctypes.data
+    kv = zp.zp_kv_pool(ptr, 16)
+    meta = zp.zp_seq_meta(R, 129, ptr, ptr, ptr, 0, None, 0, 0)
+    ws = np.zeros(4096, np.uint8)
+    wsp = (ws.ctypes.data + 255) // 256 * 256
+    for nbytes, expect in ((256, zp.ZP_ERR_INVALID_ARG), (511 + 256, zp.ZP_ERR_INVALID_ARG)):
+        st = zp.lib.zp_compress(ctypes.byref(kv), ctypes.c_void_p(ptr), ctypes.byref(meta), ctypes.c_void_p(ptr),
+                                1, ctypes.c_void_p(ptr), ctypes.byref(zp.make_params(p)), None,
+                                ctypes.c_void_p(wsp), nbytes, None)
+        assert st == expect
+    assert not host.any() and not ws.any()
 
 
 def test_commit_after_prefill_releases_every_block_past_n_max_minus_1(zp):
