@@ -266,6 +266,23 @@ zp_status zp_test_decode_stalled(const zp_kv_pool* pool, int32_t layer, const ui
                                  void* workspace, size_t workspace_bytes, int64_t stall_limit_ns,
                                  zp_stream stream);
 
+/* Test hook of the same kind for the compression pass.  Not for production use.  Same
+ * operation, arguments and workspace as zp_compress (no debug outputs), plus stall_limit_ns
+ * (1 .. 10^9); meta->max_seq_len must exceed 4096, so that the call takes the multi-pass form,
+ * whose CTAs exchange nothing with one another (ZP_ERR_INVALID_ARG otherwise).  Before its first
+ * chunk, thread 0 of every CTA of the statistics launch first waits, for at most stall_limit_ns,
+ * on a shared-memory barrier that nothing ever completes.  That wait runs out, and the CTA then
+ * takes the path of any wait that gives up: its chunks get empty row statistics, it waits
+ * (bounded, 2 s) for the copy it has in flight and records ZP_ERR_TIMEOUT in the error word.
+ * The later launches of the call run as usual, so, as for any ZP_ERR_TIMEOUT, the pool rows and
+ * global scores of the call's units are undefined afterwards; nothing is written outside the
+ * call's buffers.  Nothing faults or hangs, and the context stays usable.  Returns ZP_OK once
+ * queued. */
+zp_status zp_test_compress_stalled(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
+                                   const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
+                                   const zp_params* params, void* workspace, size_t workspace_bytes,
+                                   int64_t stall_limit_ns, zp_stream stream);
+
 /* Synchronises `stream`, copies the error word at the start of `workspace` to *out_status and
  * clears it.  Returns ZP_ERR_CUDA if the copy fails. */
 zp_status zp_read_error(void* workspace, zp_stream stream, zp_status* out_status);

@@ -804,11 +804,12 @@ extern "C" size_t zp_compress_workspace_size(const zp_params* p, int32_t num_req
                                            static_cast<int>(L));
 }
 
-extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
-                                 const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
-                                 const zp_params* p, const zp_debug* dbg, void* workspace,
-                                 size_t workspace_bytes, zp_stream stream) {
-  zp::NvtxRange nvtx_range("zp_compress");
+namespace {
+// The compression call; stall_ns != 0 only from the test hook (multi-pass form).
+zp_status compress_call(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
+                        const uint16_t* obs_q, int32_t num_qslots, float* global_scores, const zp_params* p,
+                        const zp_debug* dbg, void* workspace, size_t workspace_bytes, zp_stream stream,
+                        uint64_t stall_ns) {
   if (!pool || !meta || !obs_q || !global_scores || !p || !workspace) return ZP_ERR_INVALID_ARG;
   if (!pool->base || pool->num_blocks <= 0) return ZP_ERR_INVALID_ARG;
   // with no request the per-request arrays may be empty (NULL)
@@ -904,6 +905,7 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
   a.block_bytes = 2 * a.kv_bytes;
   a.protect_window = p->protect_window;
   a.causal = p->causal;
+  a.stall_ns = stall_ns;
 
   const ClusterPlan plan = cluster_plan(L, k, b, meta->n_max_per_req != nullptr);
   const int C = plan.C, c_lo = plan.c_lo;
@@ -926,6 +928,27 @@ extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_ta
     if (stc != ZP_OK) return stc;
   }
   return ZP_OK;
+}
+}  // namespace
+
+extern "C" zp_status zp_compress(const zp_kv_pool* pool, const int32_t* block_tables, const zp_seq_meta* meta,
+                                 const uint16_t* obs_q, int32_t num_qslots, float* global_scores,
+                                 const zp_params* p, const zp_debug* dbg, void* workspace,
+                                 size_t workspace_bytes, zp_stream stream) {
+  zp::NvtxRange nvtx_range("zp_compress");
+  return compress_call(pool, block_tables, meta, obs_q, num_qslots, global_scores, p, dbg, workspace, workspace_bytes,
+                       stream, 0);
+}
+
+extern "C" zp_status zp_test_compress_stalled(const zp_kv_pool* pool, const int32_t* block_tables,
+                                              const zp_seq_meta* meta, const uint16_t* obs_q, int32_t num_qslots,
+                                              float* global_scores, const zp_params* p, void* workspace,
+                                              size_t workspace_bytes, int64_t stall_limit_ns, zp_stream stream) {
+  if (stall_limit_ns < 1 || stall_limit_ns > 1000000000) return ZP_ERR_INVALID_ARG;
+  // the multi-pass form only: its CTAs exchange nothing, so a wait that gives up stays local
+  if (!meta || !p || meta->max_seq_len <= kMaxCluster * kKeysPerCta) return ZP_ERR_INVALID_ARG;
+  return compress_call(pool, block_tables, meta, obs_q, num_qslots, global_scores, p, nullptr, workspace,
+                       workspace_bytes, stream, static_cast<uint64_t>(stall_limit_ns));
 }
 
 extern "C" int32_t zp_compress_kernel_launches(const zp_params* p, int32_t max_seq_len, int32_t per_request_budgets) {

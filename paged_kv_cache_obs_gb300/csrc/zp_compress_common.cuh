@@ -47,6 +47,8 @@ struct CompressArgs {
   uint32_t row_bytes;             // d * 2
   int b_shift;                    // log2(b)
   int protect_window, causal;
+  uint64_t stall_ns;              // test hook (multi-pass form only): 0, or the limit of a wait
+                                  // that nothing completes, made at the start of the statistics
 };
 
 __device__ __forceinline__ float ex2(float x) {

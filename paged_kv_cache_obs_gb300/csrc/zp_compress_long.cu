@@ -45,6 +45,7 @@ struct __align__(1024) LongSmem {
   float row_off[kRows];
   float inv_n[kKeysPerCta];
   uint64_t bar_tma, bar_mma;
+  uint64_t bar_never;  // completed by nothing: the test hook's stalled wait
   uint32_t tmem_base;
 };
 
@@ -136,6 +137,7 @@ __device__ __forceinline__ bool group_prologue(LongSmem& s, const CompressArgs& 
   if (tid == 0) {
     mbar_init(&s.bar_tma, 1);
     mbar_init(&s.bar_mma, 1);
+    mbar_init(&s.bar_never, 1);
     fence_mbar_init();
   }
   for (int i = a.Rw * 8 + tid; i < kRows * 8; i += kThreads) {  // padding rows of Q are zero
@@ -192,7 +194,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nblk = (nk + a.b - 1) >> a.b_shift;
     const int nblk_next = c + 1 < c1 ? (chunk_keys(m, c + 1) + a.b - 1) >> a.b_shift : 0;
     if (tid == 0) {
-      ok = mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
+      // (the test hook first waits, for a.stall_ns, on a barrier that nothing completes: the
+      // wait gives up and the CTA takes its timeout path with the chunk's copy in flight)
+      ok = (a.stall_ns == 0 || c != c0 || mbar_wait_bounded(&s.bar_never, 0u, a.stall_ns)) &&
+           mbar_wait_bounded(&s.bar_tma, ph_tma, kWaitNs);
       if (ok) {
         ph_tma ^= 1;
         tma_pending = false;

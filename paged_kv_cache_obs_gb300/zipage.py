@@ -81,6 +81,8 @@ def _sig(name, res, args):
 _sig("zp_compress", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta), _P, _I32, _P,
                            ctypes.POINTER(zp_params), ctypes.POINTER(zp_debug), _P, _SZ, _P])
 _sig("zp_compress_workspace_size", _SZ, [ctypes.POINTER(zp_params), _I32, _I32])
+_sig("zp_test_compress_stalled", _I32, [ctypes.POINTER(zp_kv_pool), _P, ctypes.POINTER(zp_seq_meta), _P, _I32, _P,
+                                        ctypes.POINTER(zp_params), _P, _SZ, _I64, _P])
 _sig("zp_compress_kernel_launches", _I32, [ctypes.POINTER(zp_params), _I32, _I32])
 _sig("zp_paged_decode_attn", _I32, [ctypes.POINTER(zp_kv_pool), _I32, _P, _P, _P, _I32, _I32, _P,
                                     ctypes.POINTER(zp_params), _P, _SZ, _P])
@@ -204,6 +206,22 @@ def zp_compress(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_sc
                          ctypes.byref(dbg) if dbg is not None else None, _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check("zp_compress", st)
+
+
+def zp_test_compress_stalled(pool, block_tables, seq_len, qslot, dst_tables, obs_q, global_scores, params: dict,
+                             workspace, stall_limit_ns: int, max_seq_len: int, stream=None, n_max_per_req=None):
+    """Test hook of the bounded waits: the multi-pass compression (max_seq_len > 4096) whose
+    statistics CTAs first wait, at most stall_limit_ns, on a barrier nothing completes, and so
+    report ZP_ERR_TIMEOUT."""
+    kv = zp_kv_pool(pool.data_ptr(), pool.shape[1])
+    meta = zp_seq_meta(block_tables.shape[0], block_tables.shape[1], seq_len.data_ptr(),
+                       qslot.data_ptr(), dst_tables.data_ptr(), max_seq_len,
+                       None if n_max_per_req is None else n_max_per_req.data_ptr(), 0, 0)
+    st = lib.zp_test_compress_stalled(ctypes.byref(kv), _ptr(block_tables), ctypes.byref(meta), _ptr(obs_q),
+                                      obs_q.shape[0], _ptr(global_scores), ctypes.byref(make_params(params)),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      int(stall_limit_ns), _stream(stream))
+    _check("zp_test_compress_stalled", st)
 
 
 # ------------------------------------------------------------------ all-pairs redundancy -----

@@ -2,13 +2,15 @@
 
 Every wait inside the kernels is bounded; a wait that runs out makes the kernel finish its
 in-flight copies, record ZP_ERR_TIMEOUT in the error word and return, so the context stays
-usable.  zp_test_decode_stalled makes the decode kernel wait, briefly, on a barrier that nothing
-ever completes, so that this path runs for real: the test checks the reported status, that no
-write leaves its buffer, and that the next ordinary call on the same context is correct."""
+usable.  zp_test_decode_stalled and zp_test_compress_stalled make the decode kernel and the
+multi-pass compression's statistics kernel wait, briefly, on a barrier that nothing ever
+completes, so that this path runs for real: the tests check the reported status, that no write
+leaves its buffer, and that the next ordinary call on the same context is correct."""
 import numpy as np
 import pytest
 import torch
 
+from oracle import parity
 from oracle import zipage_oracle as O
 from paged_kv_cache_obs_gb300 import synth
 
@@ -93,3 +95,51 @@ def test_stall_limit_is_validated(zipage):
         with pytest.raises(zipage.ZipageError) as e:
             zipage.zp_test_decode_stalled(pool, 0, q, tables, seq, out, p, ws, stall_limit_ns=bad)
         assert e.value.status == zipage.ZP_ERR_INVALID_ARG
+
+
+def test_compression_wait_that_runs_out_reports_timeout_and_context_survives(zipage):
+    # the multi-pass form (a launch length above 4096): its CTAs exchange nothing, so a wait that
+    # gives up stays inside its CTA
+    from paged_kv_cache_obs_gb300 import runner
+    wl = synth.WORKLOADS["prefill"].scaled(num_requests=2, num_layers=1, num_kv_heads=2, num_q_heads=8,
+                                           n_max=64, prefill_max=5000)
+    inp = synth.make_inputs(wl, "cpu")
+    R = inp.num_compress
+    pool_in = synth.bf16_bits(inp.pool)
+    gs_in = inp.global_scores.numpy().copy()
+    obs_q = synth.bf16_bits(inp.obs_q)
+    batch = runner.CompressionBatch(inp, "cuda")
+    assert batch.max_seq_len > 4096
+    pristine, gs0 = batch.pool.clone(), batch.gs.clone()
+    ws, wband = _banded(zipage.zp_compress_workspace_size(batch.params, R, batch.max_seq_len))
+    with pytest.raises(zipage.ZipageError):  # only the multi-pass form takes the hook
+        zipage.zp_test_compress_stalled(batch.pool, batch.d_tables, batch.d_seq, batch.d_qslot, batch.d_dst,
+                                        batch.obs_q, batch.gs, batch.params, ws, stall_limit_ns=2_000_000,
+                                        max_seq_len=4096)
+    zipage.zp_test_compress_stalled(batch.pool, batch.d_tables, batch.d_seq, batch.d_qslot, batch.d_dst,
+                                    batch.obs_q, batch.gs, batch.params, ws, stall_limit_ns=2_000_000,
+                                    max_seq_len=batch.max_seq_len)
+    assert zipage.zp_read_error(ws) == zipage.ZP_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert bool((wband == CANARY).all())
+    # blocks outside every table of the call are untouched
+    used = set(batch.tables.ravel().tolist()) | set(batch.dst_tables.ravel().tolist())
+    others = [blk for blk in range(inp.pool.shape[1]) if blk not in used]
+    assert torch.equal(batch.pool[:, others].view(torch.int16), pristine[:, others].view(torch.int16))
+
+    # the context is intact: the ordinary call on the restored inputs matches the oracle
+    batch.pool.copy_(pristine)
+    batch.gs.copy_(gs0)
+    batch.workspace = ws
+    batch.enable_debug()
+    batch.launch()
+    assert batch.error() == 0
+    torch.cuda.synchronize()
+    assert bool((wband == CANARY).all())
+    units = [(r, l, h) for r in range(R) for l in range(wl.num_layers) for h in range(wl.num_kv_heads)]
+    dbg = {k: v.cpu().numpy() for k, v in batch.debug.items()}
+    ndiff = parity.check_units(units, pool_in, obs_q, gs_in, batch.tables, batch.dst_tables, inp.seq_len[:R],
+                               inp.qslot, wl.params(), dbg, batch.gs.cpu().numpy(), synth.bf16_bits(batch.pool),
+                               full_pool=True, n_max_per_req=inp.n_max_req)
+    assert ndiff <= 2
+    batch.close()
