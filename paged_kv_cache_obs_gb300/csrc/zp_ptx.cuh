@@ -206,15 +206,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
 // Ties a second register block to the preceding wait (no instruction emitted).
 __device__ __forceinline__ void tmem_ld_dep(uint32_t (&r)[32]) { asm volatile("" : ZP_R32(r) : : "memory"); }
 
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes: thread (lane) gets row lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  tmem_ld32_issue(taddr, r);
-  tmem_wait_ld(r);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // ------------------------------------------------------------------ clusters ------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -227,15 +218,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
-}
-
-// The two halves of a cluster barrier: work placed between them overlaps the wait for the
-// other CTAs.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ warp-level MMA ------
@@ -277,10 +259,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t local_addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
   return r;
-}
-
-__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
 // Non-blocking store of two floats to shared memory of a CTA of the cluster (`addr` from mapa);
