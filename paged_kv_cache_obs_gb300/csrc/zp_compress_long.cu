@@ -25,6 +25,10 @@
 namespace zp {
 namespace {
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 constexpr int kMaxLongL = 16384;
 constexpr int kSelThreads = 1024;
 
@@ -386,11 +390,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // 3. Selection, destinations and the global-score update, one CTA per unit.
 __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const CompressArgs a, const LongScratch sc) {
-  constexpr int kPer = kMaxLongL / kSelThreads;  // keys per thread (contiguous positions)
+  constexpr int kPer = kMaxLongL / kSelThreads;  // keys per thread: positions tid + e * kSelThreads
   __shared__ unsigned hist[256];
   __shared__ unsigned long long sh_prefix, sh_key;
   __shared__ unsigned sh_rank, sh_count;
-  __shared__ int warp_sum[kSelThreads / 32];
+  constexpr int kSelWarps = kSelThreads / 32;
+  static_assert(2 * kPer <= 32, "one prefetch lane per row of each array");
+  __shared__ int grp_base[kPer * kSelWarps];
+  __shared__ int row_total[kPer];
   __shared__ int bad_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = blockIdx.x;
@@ -417,12 +424,21 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
   }
   const int L = m.L, E = L - m.k_r;
   const float* S = sc.score + static_cast<int64_t>(unit) * a.L;
-  const int p0 = tid * kPer;  // this thread's positions [p0, p0 + kPer) for the destinations
+  float* G = a.gscores + ((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
+  const float* attn = sc.attn + static_cast<int64_t>(unit) * a.L;
+  // the global scores and attention masses are read only after the selection: ask L2 for them
+  // now (lane e of each warp: the 128-byte line of row e, lanes 16 - 31 the masses)
+  if (lane < 2 * kPer) {
+    const int e = lane % kPer;
+    const int t = e * kSelThreads + warp * 32;
+    if (t < L) prefetch_l2(lane < kPer ? static_cast<const void*>(G + t) : static_cast<const void*>(attn + t));
+  }
   // radix select of the E-th smallest key, 8 bits at a time from the top, until the chosen bin
   // holds a single key (with distinct scores, after 2 or 3 of the 8 passes).  The passes read
   // the scores from registers, loaded once with positions tid + e * kSelThreads (coalesced,
   // every thread busy).  (Aggregating each warp's adds per distinct bin with a match was
-  // slower.)
+  // slower, and so was holding the scores in shared memory, which frees the registers that
+  // spill at the 64-register limit of 1024 threads.)
   float sv[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
@@ -485,48 +501,59 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
     }
   }
   const unsigned long long T = prefix;  // exactly E keys are <= T (keys are distinct)
-  // destinations: j = number of kept keys before t
-  int kept_here = 0;
-  for (int e = 0; e < kPer; ++e) {
-    const int t = p0 + e;
-    if (t < L && evict_key(S[t], t) > T) ++kept_here;
-  }
-  int incl = kept_here;
+  // Destinations: j = number of kept keys before t.  Position t = tid + e * kSelThreads stays
+  // with the thread that holds its score, so every global access below is coalesced.  A warp
+  // ballot per e counts the kept keys of its 32 positions; warp e then scans row e of those
+  // counts (positions [e * kSelThreads, (e + 1) * kSelThreads) in order) and the row totals
+  // are summed along e in the write loop.
+  static_assert(kPer <= kSelWarps, "one warp per row of group counts");
+  const unsigned lt_mask = (1u << lane) - 1u;
+  unsigned kmask = 0;  // bit e: position tid + e * kSelThreads is kept
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
+  for (int e = 0; e < kPer; ++e) {
+    const int t = tid + e * kSelThreads;
+    const bool kept = t < L && evict_key(sv[e], t) > T;
+    kmask |= (kept ? 1u : 0u) << e;
+    const unsigned ball = __ballot_sync(0xffffffffu, kept);
+    if (lane == 0) grp_base[e * kSelWarps + warp] = __popc(ball);
   }
-  if (lane == 31) warp_sum[warp] = incl;
   __syncthreads();
-  int before = incl - kept_here;
-  for (int w2 = 0; w2 < warp; ++w2) before += warp_sum[w2];
+  if (warp < kPer) {
+    const int v = grp_base[warp * kSelWarps + lane];
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += x;
+    }
+    grp_base[warp * kSelWarps + lane] = incl - v;
+    if (lane == 31) row_total[warp] = incl;
+  }
+  __syncthreads();
   // global scores: every read of the unit's row before any write of it
-  float* G = a.gscores + ((static_cast<int64_t>(m.slot) * a.layers + m.layer) * a.Hkv + m.h) * a.L;
-  const float* attn = sc.attn + static_cast<int64_t>(unit) * a.L;
   float gnew[kPer];
-  int jdst[kPer];
-  int j = before;
+#pragma unroll
   for (int e = 0; e < kPer; ++e) {
-    const int t = p0 + e;
-    jdst[e] = -1;
+    const int t = tid + e * kSelThreads;
     gnew[e] = 0.0f;
-    if (t >= L) continue;
-    if (evict_key(S[t], t) > T) {
-      jdst[e] = j++;
-      gnew[e] = a.decay * G[t] + attn[t];
-    }
+    if ((kmask >> e) & 1u) gnew[e] = a.decay * G[t] + attn[t];
   }
   __syncthreads();
+  int row_base = 0;  // kept keys in the rows before e
+#pragma unroll
   for (int e = 0; e < kPer; ++e) {
-    const int t = p0 + e;
-    if (t >= a.L) break;
-    if (t >= L) continue;
-    if (jdst[e] >= 0) {
-      src[jdst[e]] = t;
-      G[jdst[e]] = gnew[e];
+    const int t = tid + e * kSelThreads;
+    if (e * kSelThreads >= L) break;  // uniform over the CTA
+    const bool kept = (kmask >> e) & 1u;
+    const unsigned ball = __ballot_sync(0xffffffffu, kept);
+    if (kept) {
+      const int j = row_base + grp_base[e * kSelWarps + warp] + __popc(ball & lt_mask);
+      src[j] = t;
+      G[j] = gnew[e];
     }
-    if (a.dbg_keep) a.dbg_keep[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t] = jdst[e] >= 0;
+    if (a.dbg_keep && t < L)
+      a.dbg_keep[((static_cast<int64_t>(m.r) * a.layers + m.layer) * a.Hkv + m.h) * a.L + t] = kept;
+    row_base += row_total[e];
   }
   __syncthreads();
   for (int t = m.k_r + tid; t < L; t += kSelThreads) G[t] = 0.0f;  // slots past the k survivors
