@@ -560,18 +560,23 @@ __global__ void __launch_bounds__(kSelThreads) long_select_kernel(const Compress
 }
 
 // 4. In-place compaction of the moved K and V rows, one CTA per unit, 32 destination slots at a
-//    time (small chunks keep the registers low enough for four CTAs per SM).  A row only moves to a lower slot (dst <= src), so the sources of the slots past a
-//    chunk all lie past that chunk: chunk by chunk in increasing order, with every read of a
-//    chunk before any of its writes, is a safe order, and every chunk is full of kept rows.
-//    The loads of chunk c + 1 may run ahead of the writes of chunk c (they read past them), so
-//    the kernel keeps two chunks in registers: while chunk c is written, chunk c + 1 is in
-//    flight.  Per-row byte offsets (source and destination, or -1 for a row that stays) are
-//    computed two chunks ahead into a ring of four buffers (a buffer is refilled only after
-//    the barrier that follows the writes that used it).
+//    time (small chunks keep the registers low enough for four CTAs per SM).  A row only moves
+//    to a lower slot (dst <= src), so the sources of the slots past a chunk all lie past that
+//    chunk: chunk by chunk in increasing order, with every read of a chunk before any of its
+//    writes, is a safe order, and every chunk is full of kept rows.  The loads of chunk c + 1
+//    may run ahead of the writes of chunk c (they read past them), so the kernel keeps two
+//    chunks in registers: while chunk c is written, chunk c + 1 is in flight.
+//    Per-row byte offsets (source and destination, or -1 for a row that stays) take two
+//    dependent loads (the slot's source position, then the block ids).  Every thread computes
+//    those of one slot, for a group of kThreads slots (8 chunks) at once, into one of two
+//    buffers: group g + 1 during the second chunk of group g, after the barrier that follows
+//    the last writes of group g - 1 (the buffer's previous user).  The load latency is then
+//    paid once per group instead of once per chunk.
 __global__ void __launch_bounds__(kThreads, 4) long_compact_kernel(const CompressArgs a, const LongScratch sc) {
   constexpr int kRowsC = 32;                                  // destination slots per chunk
   constexpr int kPerC = kRowsC * 2 * 128 / 8 / kThreads;      // 16-byte pieces per thread at d = 128
-  __shared__ long long src_off[4][kRowsC], dst_off[4][kRowsC];
+  constexpr int kChunksG = kThreads / kRowsC;                 // chunks per group of offsets
+  __shared__ long long src_off[2][kThreads], dst_off[2][kThreads];
   const int tid = threadIdx.x;
   const int unit = blockIdx.x;
   const UnitMeta m = unit_meta(a, unit);
@@ -586,63 +591,69 @@ __global__ void __launch_bounds__(kThreads, 4) long_compact_kernel(const Compres
   const int pieces = 2 * half;     // K then V
   const int total = kRowsC * pieces;
   const int nchunks = (m.k_r + kRowsC - 1) / kRowsC;
-  auto offsets = [&](int c) {  // threads 0..kRowsC-1: byte offsets of the slots of chunk c
-    if (tid < kRowsC) {
-      const int j = c * kRowsC + tid;
-      long long so = -1, dso = -1;
-      if (j < m.k_r) {
-        const int t = src[j];  // -1 for a reported unit
-        if (t >= 0) {
-          const int sb = src_tab[t >> a.b_shift], db = dst_tab[j >> a.b_shift];
-          if (sb != db || (t & bm) != (j & bm)) {
-            so = static_cast<long long>(static_cast<uint32_t>(sb)) * a.block_bytes + static_cast<uint32_t>(t & bm) * a.row_bytes;
-            dso = static_cast<long long>(static_cast<uint32_t>(db)) * a.block_bytes + static_cast<uint32_t>(j & bm) * a.row_bytes;
-          }
+  auto offsets = [&](int g) {  // every thread: the byte offsets of slot g * kThreads + tid
+    const int j = g * kThreads + tid;
+    long long so = -1, dso = -1;
+    if (j < m.k_r) {
+      const int t = src[j];  // -1 for a reported unit
+      if (t >= 0) {
+        const int sb = src_tab[t >> a.b_shift], db = dst_tab[j >> a.b_shift];
+        if (sb != db || (t & bm) != (j & bm)) {
+          so = static_cast<long long>(static_cast<uint32_t>(sb)) * a.block_bytes + static_cast<uint32_t>(t & bm) * a.row_bytes;
+          dso = static_cast<long long>(static_cast<uint32_t>(db)) * a.block_bytes + static_cast<uint32_t>(j & bm) * a.row_bytes;
         }
       }
-      src_off[c & 3][tid] = so;
-      dst_off[c & 3][tid] = dso;
+    }
+    src_off[g & 1][tid] = so;
+    dst_off[g & 1][tid] = dso;
+  };
+  auto refill = [&](int c) {  // during the second chunk of group g >= 1: group g + 1
+    if (c % kChunksG == 1 && c > kChunksG) {
+      const int g = c / kChunksG + 1;
+      if (g * kThreads < m.k_r) offsets(g);
     }
   };
   auto load = [&](uint4 (&v)[kPerC], int c) {
+    const long long* so_c = &src_off[(c / kChunksG) & 1][(c % kChunksG) * kRowsC];
 #pragma unroll
     for (int q = 0; q < kPerC; ++q) {
       const int i = tid + q * kThreads;
       v[q] = make_uint4(0u, 0u, 0u, 0u);
       if (i < total) {
         const int row = i / pieces, pc = i % pieces;
-        const long long so = src_off[c & 3][row];
+        const long long so = so_c[row];
         if (so >= 0) v[q] = *reinterpret_cast<const uint4*>(head_base + so + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16);
       }
     }
   };
   auto store = [&](const uint4 (&v)[kPerC], int c) {
+    const long long* dso_c = &dst_off[(c / kChunksG) & 1][(c % kChunksG) * kRowsC];
 #pragma unroll
     for (int q = 0; q < kPerC; ++q) {
       const int i = tid + q * kThreads;
       if (i < total) {
         const int row = i / pieces, pc = i % pieces;
-        const long long dso = dst_off[c & 3][row];
+        const long long dso = dso_c[row];
         if (dso >= 0) *reinterpret_cast<uint4*>(head_base + dso + (pc >= half ? a.kv_bytes : 0u) + (pc % half) * 16) = v[q];
       }
     }
   };
   if (nchunks == 0) return;
   offsets(0);
-  if (nchunks > 1) offsets(1);
+  if (kThreads < m.k_r) offsets(1);
   __syncthreads();
   uint4 va[kPerC], vb[kPerC];
   load(va, 0);
   for (int c = 0; c < nchunks; c += 2) {
     // chunk c is in va
     if (c + 1 < nchunks) load(vb, c + 1);
-    if (c + 2 < nchunks) offsets(c + 2);
+    refill(c);
     __syncthreads();  // every read of chunk c precedes every write landing on it
     store(va, c);
     if (c + 1 >= nchunks) break;
     // chunk c + 1 is in vb
     if (c + 2 < nchunks) load(va, c + 2);
-    if (c + 3 < nchunks) offsets(c + 3);
+    refill(c + 1);
     __syncthreads();
     store(vb, c + 1);
   }
