@@ -104,6 +104,10 @@ SMALL = {
                                                         global_init="uniform"),
     "multipass_gq7": synth.WORKLOADS["qwen2_7b"].scaled(num_requests=1, num_layers=1, num_q_heads=14,
                                                         num_kv_heads=2, n_max=160),
+    # the multi-pass compaction computes its row offsets 256 slots at a time: k = 4096 kept
+    # slots end exactly on such a group (L = 4112, E = 16)
+    "multipass_k_on_group": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
+                                                                num_q_heads=8, n_max=257),
 }
 
 
