@@ -261,7 +261,7 @@ def run_ours(args):
 
     peak, peak_kind = hbm_peak()
     achieved = alg_bytes / (ms / 1e3) / 1e9
-    traffic = _ncu_traffic(args.workload)
+    traffic = _ncu_traffic(args.workload, compressions * wl.num_kv_heads)
     # sequences beyond one cluster (longer than 4096 tokens) take the multi-pass form: four
     # launches per pass (its K is read twice; the algorithmic bytes count it once)
     multipass = (batch.max_seq_len or wl.L) > 4096
@@ -406,14 +406,15 @@ def compress_source_sha256():
     return h.hexdigest()
 
 
-def _ncu_traffic(workload):
-    """DRAM bytes per launch of compress_kernel from the committed ncu summary, if it exists
-    and was taken on the current kernel source (else null)."""
+def _ncu_traffic(workload, units):
+    """DRAM bytes per launch of compress_kernel from the committed ncu summary, if it exists,
+    was taken on the current kernel source and covers a launch of this many units (the
+    workload at its full size); else null."""
     path = os.path.join(ROOT, "profiles", f"compress_kernel_{workload}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        if rec.get("source_sha256") != compress_source_sha256():
+        if rec.get("source_sha256") != compress_source_sha256() or rec.get("units_full_launch") != units:
             return None
         return rec.get("dram_bytes_per_launch")
     except (OSError, ValueError):

@@ -1,6 +1,7 @@
 """Multi-rank host logic of the benchmark on CPU (gloo, world size 2): every rank contributes
 its own step time and the job time is the maximum over ranks; units are independent per rank
 (data-parallel by request), so no data-path collective exists to test."""
+import json
 import os
 import socket
 
@@ -57,3 +58,16 @@ def test_traffic_record_key_ignores_comments_only():
     assert bench._code_lines(src.replace("one", "two")) == bench._code_lines(src)
     assert bench._code_lines(src.replace("= 1", "= 2")) != bench._code_lines(src)
     assert len(bench.compress_source_sha256()) == 64
+
+
+def test_traffic_record_applies_only_to_its_launch_size():
+    # the committed record covers the full 16384-unit launch of the llama3_8b workload; a
+    # scaled-down run (fewer requests or layers) must not report it as its own traffic
+    import bench
+    with open(os.path.join(bench.ROOT, "profiles", "compress_kernel_llama3_8b_traffic.json")) as f:
+        rec = json.load(f)
+    units = rec["units_full_launch"]
+    want = rec["dram_bytes_per_launch"] if rec["source_sha256"] == bench.compress_source_sha256() else None
+    assert bench._ncu_traffic("llama3_8b", units) == want
+    assert bench._ncu_traffic("llama3_8b", units // 8) is None
+    assert bench._ncu_traffic("no_such_workload", units) is None
