@@ -108,6 +108,13 @@ SMALL = {
     # slots end exactly on such a group (L = 4112, E = 16)
     "multipass_k_on_group": synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
                                                                 num_q_heads=8, n_max=257),
+    # the multi-pass form with per-request budgets (N_max_r in 200..300, so L_r = 3200..4800
+    # on both sides of one cluster's 4096 keys) and with shared prefix blocks that the plan
+    # replaces by target blocks
+    "multipass_budgets": synth.WORKLOADS["llama3_8b"].scaled(num_requests=4, num_layers=1, num_kv_heads=2,
+                                                             num_q_heads=8, n_max=300, budget_min=200),
+    "multipass_prefix": synth.WORKLOADS["shared_prefix"].scaled(num_requests=3, num_layers=1, num_kv_heads=2,
+                                                                num_q_heads=8, n_max=300),
 }
 
 
