@@ -115,6 +115,12 @@ SMALL = {
                                                              num_q_heads=8, n_max=300, budget_min=200),
     "multipass_prefix": synth.WORKLOADS["shared_prefix"].scaled(num_requests=3, num_layers=1, num_kv_heads=2,
                                                                 num_q_heads=8, n_max=300),
+    # shared prefix blocks with lengths that differ (the grouped launches of the fused pass), and
+    # with 16-CTA clusters
+    "prefill_prefix": synth.WORKLOADS["shared_prefix"].scaled(num_requests=4, num_layers=1, num_kv_heads=2,
+                                                              num_q_heads=8, n_max=32, prefill_max=1500),
+    "long_prefix": synth.WORKLOADS["shared_prefix"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
+                                                           num_q_heads=8, n_max=200),
 }
 
 
