@@ -121,6 +121,10 @@ SMALL = {
                                                               num_q_heads=8, n_max=32, prefill_max=1500),
     "long_prefix": synth.WORKLOADS["shared_prefix"].scaled(num_requests=2, num_layers=1, num_kv_heads=2,
                                                            num_q_heads=8, n_max=200),
+    # per-request budgets from 20 to 200 blocks: length groups of 2 to 13 CTAs in one call, so
+    # both cluster widths (up to 8, and 16) run side by side
+    "long_budgets": synth.WORKLOADS["llama3_8b"].scaled(num_requests=6, num_layers=1, num_kv_heads=2,
+                                                        num_q_heads=8, n_max=200, budget_min=20),
 }
 
 
