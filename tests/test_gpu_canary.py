@@ -1,6 +1,8 @@
 """Out-of-bounds write checks (a stand-in for a memory sanitiser): every workspace is followed by
-a canary band that no call may touch, and the slots of the global scores and of the per-token
-outputs past each request's length stay as they were."""
+a canary band, and the KV pool, the global scores and the outputs lie between two bands, that
+no call may touch; the global scores of idle query slots and the slots of the global scores and
+of the per-token outputs past each request's length stay as they were, and calls that only read
+the pool leave it unchanged."""
 import numpy as np
 import pytest
 import torch
@@ -30,7 +32,24 @@ def _banded(nbytes):
     return buf[:n], buf[n:]
 
 
+def _fenced_copy(t):
+    """A device copy of tensor t between two canary bands; returns (copy, bands).  The copy
+    starts 256-byte aligned, as every buffer the library takes must be 16-byte aligned."""
+    nbytes = t.numel() * t.element_size()
+    n = (nbytes + 255) // 256 * 256
+    buf = torch.full((BAND + n + BAND,), CANARY, dtype=torch.uint8, device="cuda")
+    view = buf[BAND:BAND + nbytes].view(t.dtype).view(t.shape)
+    view.copy_(t.to("cuda"))
+    return view, (buf[:BAND], buf[BAND + n:])
+
+
+def _intact(bands):
+    return all(bool((b == CANARY).all()) for b in bands)
+
+
 @pytest.mark.parametrize("name,wl", [
+    ("trigger", synth.WORKLOADS["llama3_8b"].scaled(num_requests=2, num_layers=2)),
+    ("prefix", synth.WORKLOADS["shared_prefix"].scaled(num_requests=3, num_layers=1, num_kv_heads=2, num_q_heads=8)),
     ("prefill_small", synth.WORKLOADS["prefill"].scaled(num_requests=4, num_layers=2, n_max=32, prefill_max=1100)),
     ("long_prefill", synth.WORKLOADS["prefill"].scaled(num_requests=4, num_layers=1, num_kv_heads=2, num_q_heads=8,
                                                        n_max=64, prefill_max=4000)),
@@ -40,7 +59,9 @@ def _banded(nbytes):
 def test_compress_writes_stay_in_bounds(zp, name, wl):
     zipage, runner = zp
     inp = synth.make_inputs(wl, "cpu")
-    batch = runner.CompressionBatch(inp, "cuda")
+    pool, pool_bands = _fenced_copy(inp.pool)  # the KV pool and the global scores between bands
+    batch = runner.CompressionBatch(inp, "cuda", pool=pool)
+    batch.gs, gs_bands = _fenced_copy(inp.global_scores)
     batch.enable_debug()
     for v in batch.debug.values():
         v.fill_(-7)
@@ -52,8 +73,13 @@ def test_compress_writes_stay_in_bounds(zp, name, wl):
     assert batch.error() == 0
     torch.cuda.synchronize()
     assert bool((band == CANARY).all()), "a write past the workspace"
+    assert _intact(pool_bands), "a write outside the KV pool"
+    assert _intact(gs_bands), "a write outside the global scores"
     gs_after = batch.gs.cpu().numpy()
     gsb = gs_before.cpu().numpy()
+    # the query slots of no compressing request keep their global scores
+    idle = sorted(set(range(gsb.shape[0])) - {int(x) for x in inp.qslot[:R]})
+    assert np.array_equal(gs_after[idle], gsb[idle]), "global scores of an idle query slot"
     dbg = {k: v.cpu().numpy() for k, v in batch.debug.items()}
     for r in range(R):
         L, s = int(inp.seq_len[r]), int(inp.qslot[r])
@@ -77,16 +103,20 @@ def test_decode_and_all_pairs_workspaces_stay_in_bounds(zp):
     p = dict(num_layers=layers, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=b, n_max=mb,
              window=1, alpha=0.5, beta=0.5, decay=0.9, scale=1.0 / np.sqrt(d), protect_window=1, causal=1)
     q = torch.randn((B, Hq, d), generator=g).to(torch.bfloat16).cuda()
-    out = torch.zeros_like(q)
+    out, out_bands = _fenced_copy(torch.zeros((B, Hq, d), dtype=torch.bfloat16))
+    pool_in = pool.clone()
     ws, band = _banded(zipage.zp_paged_decode_workspace_size(p, B, mb))
     zipage.zp_paged_decode_attn(pool, 1, q, tables, seq, out, p, ws)
     assert zipage.zp_read_error(ws) == 0
     torch.cuda.synchronize()
     assert bool((band == CANARY).all()), "decode wrote past its workspace"
-    red = torch.full((B, layers, Hkv, mb * b), -7.0, device="cuda")
+    assert _intact(out_bands), "decode wrote outside its output"
+    red, red_bands = _fenced_copy(torch.full((B, layers, Hkv, mb * b), -7.0))
     ws, band = _banded(zipage.zp_redundancy_workspace_size(p, B))
     zipage.zp_redundancy_all_pairs(pool, tables, seq, red, p, ws)
     assert zipage.zp_read_error(ws) == 0
     torch.cuda.synchronize()
     assert bool((band == CANARY).all()), "all-pairs redundancy wrote past its workspace"
+    assert _intact(red_bands), "all-pairs redundancy wrote outside its output"
     assert torch.isfinite(red).all()
+    assert torch.equal(pool.view(torch.int16), pool_in.view(torch.int16)), "a read-only call wrote to the pool"
